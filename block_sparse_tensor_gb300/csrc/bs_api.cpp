@@ -1,0 +1,727 @@
+// C ABI entry points (include/bs.h): argument checks, plan construction,
+// device tables, and the launches that make up one contraction.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <new>
+#include <tuple>
+
+#include "bs_plan.h"
+
+using namespace bs;
+
+namespace {
+
+bs_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return BS_OK;
+  if (e == cudaErrorMemoryAllocation) return BS_ERR_OOM;
+  return BS_ERR_CUDA;
+}
+
+#define BS_CUDA(call)                                        \
+  do {                                                       \
+    cudaError_t e_ = (call);                                 \
+    if (e_ != cudaSuccess) return cuda_status(e_);           \
+  } while (0)
+
+Sparsity sparsity_of(const bs_layout &L) {
+  Sparsity sp;
+  sp.ptr.assign(L.rows.n + 1, 0);
+  for (int32_t r = 0; r < L.rows.n; ++r) {
+    std::vector<int32_t> cs;
+    for (int64_t t = L.row_ptr[r]; t < L.row_ptr[r + 1]; ++t) cs.push_back(L.blocks[L.row_blk[t]].col);
+    std::sort(cs.begin(), cs.end());
+    sp.cols.insert(sp.cols.end(), cs.begin(), cs.end());
+    sp.ptr[r + 1] = (int64_t)sp.cols.size();
+  }
+  return sp;
+}
+
+// Populated C blocks: (i, j) with some k holding A[i,k] and B[k,j].
+Sparsity product_sparsity(const bs_layout &A, const bs_layout &B) {
+  Sparsity sp;
+  const int32_t ni = A.rows.n, nj = B.cols.n;
+  sp.ptr.assign(ni + 1, 0);
+  std::vector<uint8_t> seen(nj, 0);
+  std::vector<int32_t> row;
+  for (int32_t i = 0; i < ni; ++i) {
+    row.clear();
+    for (int64_t t = A.row_ptr[i]; t < A.row_ptr[i + 1]; ++t) {
+      const int32_t k = A.blocks[A.row_blk[t]].col;
+      for (int64_t u = B.row_ptr[k]; u < B.row_ptr[k + 1]; ++u) {
+        const int32_t j = B.blocks[B.row_blk[u]].col;
+        if (!seen[j]) {
+          seen[j] = 1;
+          row.push_back(j);
+        }
+      }
+    }
+    std::sort(row.begin(), row.end());
+    for (int32_t j : row) seen[j] = 0;
+    sp.cols.insert(sp.cols.end(), row.begin(), row.end());
+    sp.ptr[i + 1] = (int64_t)sp.cols.size();
+  }
+  return sp;
+}
+
+int64_t populated_elems(const bs_layout &L) {
+  int64_t s = 0;
+  for (const auto &b : L.blocks) s += (int64_t)b.rows * b.cols;
+  return s;
+}
+
+// Block copies of the gather, split into row bands of at most 16K elements so
+// one huge block does not serialise the launch on a single CTA.
+void pack_list(const bs_layout &src, const bs_layout &dst, std::vector<PackCopy> *out) {
+  for (const auto &b : src.blocks) {
+    const auto &d = dst.blocks[dst.find(b.row, b.col)];
+    const int32_t band = std::max<int32_t>(1, 16384 / b.cols);
+    for (int32_t r0 = 0; r0 < b.rows; r0 += band) {
+      PackCopy c{};
+      c.src = b.offset + (int64_t)r0 * b.ld;
+      c.src_ld = b.ld;
+      c.dst = d.offset + (int64_t)r0 * d.ld;
+      c.dst_ld = d.ld;
+      c.rows = std::min(band, b.rows - r0);
+      c.cols = b.cols;
+      out->push_back(c);
+    }
+  }
+}
+
+void zero_list(const bs_layout &C, std::vector<ZeroBlock> *out) {
+  for (const auto &b : C.blocks) {
+    const int32_t band = std::max<int32_t>(1, 16384 / b.cols);
+    for (int32_t r0 = 0; r0 < b.rows; r0 += band)
+      out->push_back({b.offset + (int64_t)r0 * b.ld, b.ld, std::min(band, b.rows - r0), b.cols});
+  }
+}
+
+bool tma_ok(int64_t off, int64_t ld, int eb) { return (off * eb) % 16 == 0 && (ld * eb) % 16 == 0; }
+
+bool groups_tma_ok(const GroupSet &gs) {
+  for (const auto &s : gs.ksegs)
+    if (!tma_ok(s.ka, s.kl, 2) || !tma_ok(s.kb, s.ldb, 2)) return false;
+  return true;
+}
+
+template <class T>
+size_t append_bytes(std::vector<unsigned char> &buf, const std::vector<T> &v) {
+  size_t off = (buf.size() + 255) / 256 * 256;
+  buf.resize(off + v.size() * sizeof(T));
+  if (!v.empty()) std::memcpy(buf.data() + off, v.data(), v.size() * sizeof(T));
+  return off;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+bs_status encode_maps(bs_plan *P, const void *A, const void *B) {
+  auto enc = get_encode();
+  if (!enc) return BS_ERR_CUDA;
+  P->map_bytes.assign(P->maps.size() * sizeof(CUtensorMap), 0);
+  for (size_t t = 0; t < P->maps.size(); ++t) {
+    const MapDesc &m = P->maps[t];
+    const char *base = (const char *)(m.operand == 0 ? A : B) + m.off * 2;
+    cuuint64_t dims[2] = {(cuuint64_t)m.inner, (cuuint64_t)m.outer};
+    cuuint64_t strides[1] = {(cuuint64_t)(m.ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)m.box_inner, (cuuint32_t)m.box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUtensorMap *out = (CUtensorMap *)(P->map_bytes.data() + t * sizeof(CUtensorMap));
+    CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)base, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return BS_ERR_MISALIGNED;
+  }
+  return BS_OK;
+}
+
+// BF16 tasks: 128-row tiles of each contraction-axis group, one tensor-map
+// pair per inner segment.
+void build_bf16(bs_plan *P) {
+  const GroupSet &gs = P->gs;
+  std::map<std::tuple<int, int64_t, int64_t, int64_t, int64_t>, int32_t> seen;
+  auto map_id = [&](int op, int64_t off, int64_t inner, int64_t outer, int64_t ld, int bi, int bo) {
+    auto key = std::make_tuple(op, off, inner, outer, ld);
+    auto it = seen.find(key);
+    if (it != seen.end()) return it->second;
+    MapDesc m{op, off, inner, outer, ld, bi, bo};
+    P->maps.push_back(m);
+    int32_t id = (int32_t)P->maps.size() - 1;
+    seen[key] = id;
+    return id;
+  };
+  std::vector<std::pair<double, Bf16Task>> costed;
+  for (const auto &g : gs.groups) {
+    const RowSeg &rs = gs.rsegs[g.rseg_begin];
+    const int32_t pb = (int32_t)P->bpairs.size();
+    for (int32_t s = 0; s < g.kseg_count; ++s) {
+      const KSeg &k = gs.ksegs[g.kseg_begin + s];
+      Bf16Pair pr{};
+      pr.map_a = map_id(0, k.ka, k.klen, g.m, k.kl, 64, 128);
+      pr.map_b = map_id(1, k.kb, g.n, k.klen, k.ldb, 64, 64);
+      pr.klen = k.klen;
+      P->bpairs.push_back(pr);
+    }
+    for (int32_t m0 = 0; m0 < g.m; m0 += 128)
+      for (int32_t n0 = 0; n0 < g.n; n0 += 256) {
+        Bf16Task t{};
+        t.pair_begin = pb;
+        t.pair_count = g.kseg_count;
+        t.m0 = m0;
+        t.n0 = n0;
+        t.m = g.m;
+        t.n = g.n;
+        t.bn = (std::min(256, g.n - n0) + 15) / 16 * 16;
+        t.c_off = rs.rc;
+        t.ldc = rs.ldc;
+        int64_t kch = 0;
+        for (int32_t s = 0; s < g.kseg_count; ++s) kch += (gs.ksegs[g.kseg_begin + s].klen + 63) / 64;
+        costed.push_back({(double)kch * (t.bn + 64), t});
+      }
+  }
+  std::stable_sort(costed.begin(), costed.end(),
+                   [](const std::pair<double, Bf16Task> &a, const std::pair<double, Bf16Task> &b) { return a.first > b.first; });
+  for (auto &c : costed) P->btasks.push_back(c.second);
+}
+
+bs_status upload(bs_plan *P) {
+  std::vector<unsigned char> buf;
+  size_t o_tasks = append_bytes(buf, P->ts.tasks);
+  size_t o_groups = append_bytes(buf, P->gs.groups);
+  size_t o_rsegs = append_bytes(buf, P->gs.rsegs);
+  size_t o_ksegs = append_bytes(buf, P->gs.ksegs);
+  size_t o_tail = append_bytes(buf, P->ts.tail_groups);
+  size_t o_pack = append_bytes(buf, P->pack_copies);
+  size_t o_zero = append_bytes(buf, P->zero_blocks);
+  size_t o_bt = append_bytes(buf, P->btasks);
+  size_t o_bp = append_bytes(buf, P->bpairs);
+  std::vector<unsigned char> mapspace(P->maps.size() * sizeof(CUtensorMap), 0);
+  size_t o_maps = append_bytes(buf, mapspace);
+  size_t total = (buf.size() + 255) / 256 * 256 + 256;
+  buf.resize(total, 0);
+  BS_CUDA(cudaMalloc(&P->d_tables, total));
+  P->tables_bytes = total;
+  BS_CUDA(cudaMemcpy(P->d_tables, buf.data(), total, cudaMemcpyHostToDevice));
+  char *b = (char *)P->d_tables;
+  P->d_tasks = (Task *)(b + o_tasks);
+  P->d_groups = (Group *)(b + o_groups);
+  P->d_rsegs = (RowSeg *)(b + o_rsegs);
+  P->d_ksegs = (KSeg *)(b + o_ksegs);
+  P->d_tail = (int32_t *)(b + o_tail);
+  P->d_pack = (PackCopy *)(b + o_pack);
+  P->d_zero = (ZeroBlock *)(b + o_zero);
+  P->d_btasks = (Bf16Task *)(b + o_bt);
+  P->d_bpairs = (Bf16Pair *)(b + o_bp);
+  P->d_maps = (void *)(b + o_maps);
+  // counters and status word: zero once, kernels return them to zero
+  void *cs = nullptr;
+  BS_CUDA(cudaMalloc(&cs, 256));
+  BS_CUDA(cudaMemset(cs, 0, 256));
+  P->d_counter = (uint32_t *)cs;
+  P->d_status = (int32_t *)((char *)cs + 128);
+  const int eb = P->dtype == BS_F64 ? 8 : 2;
+  if (P->pack_a) BS_CUDA(cudaMalloc(&P->d_ws_a, std::max<int64_t>(P->A_pk.nelems, 1) * eb));
+  if (P->pack_b) BS_CUDA(cudaMalloc(&P->d_ws_b, std::max<int64_t>(P->B_pk.nelems, 1) * eb));
+  P->stats.workspace_bytes = (int64_t)total + 256 + (P->pack_a ? P->A_pk.nelems * eb : 0) +
+                             (P->pack_b ? P->B_pk.nelems * eb : 0);
+  return BS_OK;
+}
+
+void free_device(bs_plan *P) {
+  cudaFree(P->d_tables);
+  cudaFree(P->d_counter);
+  cudaFree(P->d_ws_a);
+  cudaFree(P->d_ws_b);
+  cudaFree(P->d_host_a);
+  cudaFree(P->d_host_b);
+  cudaFree(P->d_host_c);
+  P->d_tables = P->d_ws_a = P->d_ws_b = P->d_host_a = P->d_host_b = P->d_host_c = nullptr;
+  P->d_counter = nullptr;
+}
+
+struct Candidate {
+  int axis;
+  bool pack;
+  double us;
+};
+
+}  // namespace
+
+extern "C" {
+
+const char *bs_status_string(bs_status s) {
+  switch (s) {
+    case BS_OK: return "ok";
+    case BS_ERR_INVALID_ARG: return "invalid argument";
+    case BS_ERR_SHAPE_MISMATCH: return "shape mismatch";
+    case BS_ERR_UNSUPPORTED: return "unsupported";
+    case BS_ERR_OOM: return "out of memory";
+    case BS_ERR_CUDA: return "CUDA error";
+    case BS_ERR_TIMEOUT: return "device wait timed out";
+    case BS_ERR_MISALIGNED: return "misaligned buffer or view";
+    case BS_ERR_DEVICE: return "device-side check failed";
+    case BS_ERR_OVERFLOW: return "size overflow";
+  }
+  return "unknown status";
+}
+
+const char *bs_version(void) { return "bs 0.1 sm_103a"; }
+
+bs_status bs_layout_create(const bs_axis_desc *rows, const bs_axis_desc *cols, const bs_rule *rule, uint32_t flags,
+                           int32_t elem_bytes, bs_layout **out) {
+  if (!out) return BS_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!rows || !cols || !rule) return BS_ERR_INVALID_ARG;
+  if (rule->dq_min > rule->dq_max) return BS_ERR_INVALID_ARG;
+  bs_layout *L = new (std::nothrow) bs_layout();
+  if (!L) return BS_ERR_OOM;
+  AxisCopy r, c;
+  bs_status st = copy_axis(rows, &r);
+  if (st == BS_OK) st = copy_axis(cols, &c);
+  if (st == BS_OK && rule->z2 && (r.p.empty() || c.p.empty())) st = BS_ERR_INVALID_ARG;
+  if (st == BS_OK) {
+    try {
+      st = build_layout(r, c, rule_sparsity(r, c, *rule), flags, elem_bytes, L);
+    } catch (const std::bad_alloc &) {
+      st = BS_ERR_OOM;
+    }
+  }
+  if (st != BS_OK) {
+    delete L;
+    return st;
+  }
+  *out = L;
+  return BS_OK;
+}
+
+bs_status bs_layout_query(const bs_layout *L, int64_t *nblocks, int64_t *nelems) {
+  if (!L) return BS_ERR_INVALID_ARG;
+  if (nblocks) *nblocks = (int64_t)L->blocks.size();
+  if (nelems) *nelems = L->nelems;
+  return BS_OK;
+}
+
+bs_status bs_layout_blocks(const bs_layout *L, bs_block_info *out) {
+  if (!L || (!out && !L->blocks.empty())) return BS_ERR_INVALID_ARG;
+  if (!L->blocks.empty()) std::memcpy(out, L->blocks.data(), L->blocks.size() * sizeof(bs_block_info));
+  return BS_OK;
+}
+
+void bs_layout_destroy(bs_layout *L) { delete L; }
+
+void bs_plan_options_default(bs_plan_options *o) {
+  if (!o) return;
+  std::memset(o, 0, sizeof *o);
+  o->axis_policy = BS_AXIS_AUTO;
+  o->pack_policy = BS_PACK_AUTO;
+  o->c_layout_flags = BS_LAYOUT_BLOCKROW;
+  o->merge_rows = 1;
+}
+
+bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, const bs_plan_options *opts,
+                         bs_plan **out) {
+  if (!out) return BS_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!A || !B) return BS_ERR_INVALID_ARG;
+  if (dtype != BS_F64 && dtype != BS_BF16_F32) return BS_ERR_INVALID_ARG;
+  bs_plan_options o;
+  bs_plan_options_default(&o);
+  if (opts) o = *opts;
+  if (o.axis_policy < 0 || o.axis_policy > 3 || o.pack_policy < 0 || o.pack_policy > 2) return BS_ERR_INVALID_ARG;
+  if ((o.c_layout_flags & ~15u) || (o.c_layout_flags & 3u) == 3u) return BS_ERR_INVALID_ARG;
+  const int eb_in = dtype == BS_F64 ? 8 : 2;
+  if (A->elem_bytes != eb_in || B->elem_bytes != eb_in) return BS_ERR_INVALID_ARG;
+  if (!A->cols.same_as(B->rows)) return BS_ERR_SHAPE_MISMATCH;
+  if (dtype == BS_BF16_F32 && (o.axis_policy == BS_AXIS_FREE || o.axis_policy == BS_AXIS_NONE))
+    return BS_ERR_UNSUPPORTED;
+  const auto t0 = std::chrono::steady_clock::now();
+  bs_plan *P = new (std::nothrow) bs_plan();
+  if (!P) return BS_ERR_OOM;
+  bs_status st = BS_OK;
+  try {
+    P->dtype = dtype;
+    P->opts = o;
+    P->A = *A;
+    P->B = *B;
+    st = build_layout(A->rows, B->cols, product_sparsity(*A, *B), o.c_layout_flags, dtype == BS_F64 ? 8 : 4, &P->C);
+    if (st != BS_OK) {
+      delete P;
+      return st;
+    }
+    PlanModel pm;
+    if (o.t_launch_us > 0) pm.t_launch_us = o.t_launch_us;
+    if (o.t_task_us > 0) pm.t_task_us = o.t_task_us;
+    if (o.t_segment_us > 0) pm.t_segment_us = o.t_segment_us;
+    if (o.pack_gbs > 0) pm.pack_gbs = o.pack_gbs;
+    if (o.fp64_gflops > 0) pm.fp64_gflops = o.fp64_gflops;
+    if (o.atomic_penalty > 0) pm.atomic_penalty = o.atomic_penalty;
+    if (!o.host_only) {
+      int dev = 0, major = 0, minor = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess) {
+        delete P;
+        return BS_ERR_CUDA;
+      }
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+      if (major != 10 || minor != 3) {
+        delete P;
+        return BS_ERR_UNSUPPORTED;
+      }
+      P->device = dev;
+      cudaDeviceGetAttribute(&P->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    } else {
+      P->sm_count = 152;
+    }
+    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : (o.host_only ? 3 : std::max(1, fp64_max_ctas_per_sm()));
+    pm.parallel_ctas = P->sm_count * cps;
+
+    const bool sorted_pack = true;
+    auto packed = [&](const bs_layout &src, uint32_t mode, bs_layout *dst) {
+      uint32_t f = mode | (sorted_pack ? BS_LAYOUT_CHARGE_SORTED : 0) | (dtype == BS_BF16_F32 ? BS_LAYOUT_ALIGN16 : 0);
+      return build_layout(src.rows, src.cols, sparsity_of(src), f, src.elem_bytes, dst);
+    };
+
+    if (dtype == BS_F64) {
+      std::vector<int> axes;
+      if (o.axis_policy == BS_AXIS_AUTO) axes = {BS_AXIS_CONTRACTION, BS_AXIS_FREE};
+      else axes = {o.axis_policy};
+      std::vector<bool> packs;
+      if (o.pack_policy == BS_PACK_AUTO) packs = {false, true};
+      else packs = {o.pack_policy == BS_PACK_ALWAYS};
+      std::vector<Candidate> cands;
+      double best = 1e300;
+      int best_axis = -1;
+      bool best_pack = false;
+      for (int ax : axes)
+        for (bool pk : packs) {
+          if (pk && ax == BS_AXIS_NONE) continue;
+          bs_layout Apk, Bpk;
+          const bs_layout *Ae = &P->A, *Be = &P->B;
+          int64_t pbytes = 0;
+          if (pk) {
+            st = packed(P->A, ax == BS_AXIS_FREE ? BS_LAYOUT_COLPANEL : BS_LAYOUT_ROWPANEL, &Apk);
+            if (st != BS_OK) break;
+            Ae = &Apk;
+            pbytes += populated_elems(P->A) * eb_in;
+            if (ax == BS_AXIS_CONTRACTION) {
+              st = packed(P->B, BS_LAYOUT_COLPANEL, &Bpk);
+              if (st != BS_OK) break;
+              Be = &Bpk;
+              pbytes += populated_elems(P->B) * eb_in;
+            }
+          }
+          const auto tg0 = std::chrono::steady_clock::now();
+          GroupSet gs = ax == BS_AXIS_CONTRACTION ? make_contraction_groups(*Ae, *Be, P->C, o.merge_rows != 0, false)
+                        : ax == BS_AXIS_FREE      ? make_free_groups(*Ae, *Be, P->C)
+                                                  : make_triple_groups(*Ae, *Be, P->C);
+          const auto tg1 = std::chrono::steady_clock::now();
+          TileSet ts;
+          tile_fp64(gs, pm, &ts);
+          const auto tg2 = std::chrono::steady_clock::now();
+          const bool atomic = ax != BS_AXIS_CONTRACTION;
+          const int launches = 1 + (pk ? 1 : 0) + (atomic ? 1 : 0);
+          const double us = model_fp64_us(gs, ts, pm, pbytes, launches);
+          if (std::getenv("BS_LOG"))
+            std::fprintf(stderr, "[bs] candidate axis=%d pack=%d groups=%zu tasks=%zu model=%.1f us (group %.1f ms, tile %.1f ms)\n",
+                         ax, (int)pk, gs.groups.size(), ts.tasks.size(), us,
+                         std::chrono::duration<double, std::milli>(tg1 - tg0).count(),
+                         std::chrono::duration<double, std::milli>(tg2 - tg1).count());
+          cands.push_back({ax, pk, us});
+          if (us < best) {
+            best = us;
+            best_axis = ax;
+            best_pack = pk;
+            P->gs = std::move(gs);
+            P->ts = std::move(ts);
+            P->pack_a = pk;
+            P->pack_b = pk && ax == BS_AXIS_CONTRACTION;
+            if (pk) P->A_pk = Apk;
+            if (P->pack_b) P->B_pk = Bpk;
+          }
+        }
+      if (st != BS_OK) {
+        delete P;
+        return st;
+      }
+      P->axis = best_axis;
+      P->stats.model_us = best;
+      double alt = 0;
+      for (const auto &c : cands)
+        if (!(c.axis == best_axis && c.pack == best_pack)) alt = alt == 0 ? c.us : std::min(alt, c.us);
+      P->stats.model_us_alt = alt;
+      (void)best_pack;
+    } else {
+      // BF16: contraction axis; views must satisfy the tensor-map rules, else gather
+      GroupSet gs = make_contraction_groups(P->A, P->B, P->C, o.merge_rows != 0, false);
+      bool need_pack = !groups_tma_ok(gs) || o.pack_policy == BS_PACK_ALWAYS;
+      if (need_pack && o.pack_policy == BS_PACK_NEVER) {
+        delete P;
+        return BS_ERR_MISALIGNED;
+      }
+      if (need_pack) {
+        st = packed(P->A, BS_LAYOUT_ROWPANEL, &P->A_pk);
+        if (st == BS_OK) st = packed(P->B, BS_LAYOUT_COLPANEL, &P->B_pk);
+        if (st != BS_OK) {
+          delete P;
+          return st;
+        }
+        P->pack_a = P->pack_b = true;
+        gs = make_contraction_groups(P->A_pk, P->B_pk, P->C, o.merge_rows != 0, false);
+      }
+      P->gs = std::move(gs);
+      P->axis = BS_AXIS_CONTRACTION;
+      build_bf16(P);
+    }
+    if (P->pack_a) pack_list(P->A, P->A_pk, &P->pack_copies);
+    P->pack_copies_a = (int32_t)P->pack_copies.size();
+    if (P->pack_b) pack_list(P->B, P->B_pk, &P->pack_copies);
+    bool any_atomic = false;
+    for (const auto &g : P->gs.groups) any_atomic |= (g.flags & GF_ATOMIC) != 0;
+    if (any_atomic) zero_list(P->C, &P->zero_blocks);
+
+    // statistics
+    bs_plan_stats &S = P->stats;
+    std::vector<int64_t> tp;
+    std::vector<int32_t> tr;
+    group_triples(P->gs, &tp, &tr);
+    S.triples = (int64_t)tr.size() / 3;
+    double fl = 0;
+    for (size_t t = 0; t < tr.size(); t += 3)
+      fl += 2.0 * A->rows.d[tr[t]] * A->cols.d[tr[t + 1]] * B->cols.d[tr[t + 2]];
+    S.useful_flops = fl;
+    S.c_blocks = (int64_t)P->C.blocks.size();
+    S.groups = (int64_t)P->gs.groups.size();
+    int64_t nseg = 0;
+    for (const auto &g : P->gs.groups) nseg += std::max(g.kseg_count, g.rseg_count);
+    S.segments = nseg;
+    S.axis = P->axis;
+    S.packed_a = P->pack_a;
+    S.packed_b = P->pack_b;
+    S.packed_bytes = (P->pack_a ? populated_elems(P->A) * eb_in : 0) + (P->pack_b ? populated_elems(P->B) * eb_in : 0);
+    const int eb_out = dtype == BS_F64 ? 8 : 4;
+    S.useful_bytes = (double)(populated_elems(P->A) + populated_elems(P->B)) * eb_in + (double)populated_elems(P->C) * eb_out;
+    if (dtype == BS_F64) {
+      S.tasks = (int64_t)P->ts.tasks.size();
+      for (const auto &t : P->ts.tasks) (t.kind == TK_TILE ? S.tile_tasks : S.tail_tasks)++;
+      S.executed_flops = P->ts.executed_flops;
+    } else {
+      S.tasks = S.tile_tasks = (int64_t)P->btasks.size();
+      double ex = 0;
+      for (const auto &t : P->btasks) {
+        int64_t kk = 0;
+        for (int32_t s = 0; s < t.pair_count; ++s) kk += (P->bpairs[t.pair_begin + s].klen + 15) / 16 * 16;
+        ex += 2.0 * 128 * t.bn * kk;
+      }
+      S.executed_flops = ex;
+    }
+    S.launches = 1 + ((P->pack_a || P->pack_b) ? 1 : 0) + (P->zero_blocks.empty() ? 0 : 1);
+
+    if (!o.host_only) {
+      st = upload(P);
+      if (st != BS_OK) {
+        free_device(P);
+        delete P;
+        return st;
+      }
+      if (dtype == BS_F64) P->grid = std::max(1, std::min<int>((int)P->ts.tasks.size(), P->sm_count * cps));
+      else P->grid = std::max(1, std::min<int>((int)P->btasks.size(), P->sm_count));
+    }
+  } catch (const std::bad_alloc &) {
+    free_device(P);
+    delete P;
+    return BS_ERR_OOM;
+  }
+  P->stats.plan_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  *out = P;
+  return BS_OK;
+}
+
+const bs_layout *bs_plan_c_layout(const bs_plan *P) { return P ? &P->C : nullptr; }
+
+bs_status bs_plan_stats_get(const bs_plan *P, bs_plan_stats *out) {
+  if (!P || !out) return BS_ERR_INVALID_ARG;
+  *out = P->stats;
+  return BS_OK;
+}
+
+bs_status bs_plan_groups(const bs_plan *P, int64_t *ngroups, int64_t *out) {
+  if (!P || !ngroups) return BS_ERR_INVALID_ARG;
+  *ngroups = (int64_t)P->gs.groups.size();
+  if (!out) return BS_OK;
+  std::vector<int64_t> tp;
+  std::vector<int32_t> tr;
+  group_triples(P->gs, &tp, &tr);
+  for (size_t g = 0; g < P->gs.groups.size(); ++g) {
+    const Group &G = P->gs.groups[g];
+    int64_t *o = out + 8 * g;
+    o[0] = P->axis == BS_AXIS_AUTO ? BS_AXIS_CONTRACTION : P->axis;
+    o[1] = G.m;
+    o[2] = G.n;
+    o[3] = G.k;
+    o[4] = G.rseg_count;
+    o[5] = G.kseg_count;
+    o[6] = tp[g] < tp[g + 1] ? tr[3 * tp[g]] : -1;
+    o[7] = tp[g] < tp[g + 1] ? tr[3 * tp[g] + 2] : -1;
+  }
+  return BS_OK;
+}
+
+bs_status bs_plan_triples(const bs_plan *P, int64_t *ntriples, int64_t *ngroups, int64_t *group_ptr, int32_t *out) {
+  if (!P || !ntriples || !ngroups) return BS_ERR_INVALID_ARG;
+  std::vector<int64_t> tp;
+  std::vector<int32_t> tr;
+  group_triples(P->gs, &tp, &tr);
+  *ntriples = (int64_t)tr.size() / 3;
+  *ngroups = (int64_t)P->gs.groups.size();
+  if (group_ptr) std::memcpy(group_ptr, tp.data(), tp.size() * sizeof(int64_t));
+  if (out && !tr.empty()) std::memcpy(out, tr.data(), tr.size() * sizeof(int32_t));
+  return BS_OK;
+}
+
+bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *stream) {
+  if (!P) return BS_ERR_INVALID_ARG;
+  if (P->opts.host_only) return BS_ERR_INVALID_ARG;
+  if (P->C.nelems == 0) return BS_OK;
+  if (!A || !B || !C) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const void *Ause = P->pack_a ? P->d_ws_a : A;
+  const void *Buse = P->pack_b ? P->d_ws_b : B;
+  if (!P->pack_copies.empty()) {
+    PackParams pp{};
+    pp.src = A;
+    pp.dst = P->d_ws_a;
+    pp.copies = P->d_pack;
+    pp.ncopies = P->pack_copies_a;
+    pp.elem_bytes = P->dtype == BS_F64 ? 8 : 2;
+    // one launch gathers both operands: copies [0, n_a) read A, the rest read B
+    PackParams pb = pp;
+    pb.src = B;
+    pb.dst = P->d_ws_b;
+    BS_CUDA(launch_pack2(pp, pb, (int32_t)P->pack_copies.size(), P->sm_count * 4, s));
+  }
+  if (!P->zero_blocks.empty())
+    BS_CUDA(launch_zero(C, P->dtype == BS_F64 ? 8 : 4, P->d_zero, (int)P->zero_blocks.size(), P->sm_count * 4, s));
+  if (P->dtype == BS_F64) {
+    if (P->ts.tasks.empty()) return BS_OK;
+    Fp64Params p{};
+    p.A = (const double *)Ause;
+    p.B = (const double *)Buse;
+    p.C = (double *)C;
+    p.tasks = P->d_tasks;
+    p.groups = P->d_groups;
+    p.rsegs = P->d_rsegs;
+    p.ksegs = P->d_ksegs;
+    p.tail_groups = P->d_tail;
+    p.ntasks = (int32_t)P->ts.tasks.size();
+    p.counter = P->d_counter;
+    p.status = P->d_status;
+    BS_CUDA(launch_fp64_grouped(p, P->grid, s));
+  } else {
+    if (((uintptr_t)Ause | (uintptr_t)Buse | (uintptr_t)C) % 16 != 0) return BS_ERR_MISALIGNED;
+    if (P->btasks.empty()) return BS_OK;
+    if (P->maps_a_ptr != Ause || P->maps_b_ptr != Buse) {
+      bs_status st = encode_maps(P, Ause, Buse);
+      if (st != BS_OK) return st;
+      BS_CUDA(cudaMemcpyAsync(P->d_maps, P->map_bytes.data(), P->map_bytes.size(), cudaMemcpyHostToDevice, s));
+      BS_CUDA(cudaStreamSynchronize(s));
+      P->maps_a_ptr = Ause;
+      P->maps_b_ptr = Buse;
+    }
+    Bf16Params p{};
+    p.maps = P->d_maps;
+    p.tasks = P->d_btasks;
+    p.pairs = P->d_bpairs;
+    p.C = (float *)C;
+    p.ntasks = (int32_t)P->btasks.size();
+    p.status = P->d_status;
+    p.counter = P->d_counter;
+    p.timeout_ns = (uint64_t)(P->opts.wait_timeout_ms > 0 ? P->opts.wait_timeout_ms : 2000) * 1000000ull;
+    p.debug_flags = P->opts.debug_flags;
+    BS_CUDA(launch_bf16_grouped(p, P->grid, s));
+  }
+  return BS_OK;
+}
+
+bs_status bs_contract_host(bs_plan *P, const void *A_host, const void *B_host, void *C_host, void *stream) {
+  if (!P || !A_host || !B_host || !C_host || P->opts.host_only) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t eb = P->dtype == BS_F64 ? 8 : 2, ec = P->dtype == BS_F64 ? 8 : 4;
+  const size_t na = (size_t)P->A.nelems * eb, nb = (size_t)P->B.nelems * eb, nc = (size_t)P->C.nelems * ec;
+  if (!P->d_host_c) {
+    BS_CUDA(cudaMalloc(&P->d_host_a, std::max<size_t>(na, 16)));
+    BS_CUDA(cudaMalloc(&P->d_host_b, std::max<size_t>(nb, 16)));
+    BS_CUDA(cudaMalloc(&P->d_host_c, std::max<size_t>(nc, 16)));
+    BS_CUDA(cudaMemset(P->d_host_c, 0, std::max<size_t>(nc, 16)));   // padding stays zero
+  }
+  BS_CUDA(cudaMemcpyAsync(P->d_host_a, A_host, na, cudaMemcpyHostToDevice, s));
+  BS_CUDA(cudaMemcpyAsync(P->d_host_b, B_host, nb, cudaMemcpyHostToDevice, s));
+  bs_status st = bs_contract(P, P->d_host_a, P->d_host_b, P->d_host_c, stream);
+  if (st != BS_OK) return st;
+  BS_CUDA(cudaMemcpyAsync(C_host, P->d_host_c, nc, cudaMemcpyDeviceToHost, s));
+  BS_CUDA(cudaStreamSynchronize(s));
+  return BS_OK;
+}
+
+bs_status bs_contract_uncoalesced(bs_plan *P, const void *A, const void *B, void *C, void *stream) {
+  if (!P || P->opts.host_only) return BS_ERR_INVALID_ARG;
+  if (P->C.nelems == 0) return BS_OK;
+  if (!A || !B || !C) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  std::vector<int64_t> tp;
+  std::vector<int32_t> tr;
+  group_triples(P->gs, &tp, &tr);
+  const size_t ec = P->dtype == BS_F64 ? 8 : 4;
+  BS_CUDA(cudaMemsetAsync(C, 0, (size_t)P->C.nelems * ec, s));
+  for (size_t t = 0; t < tr.size(); t += 3) {
+    const auto &a = P->A.blocks[P->A.find(tr[t], tr[t + 1])];
+    const auto &b = P->B.blocks[P->B.find(tr[t + 1], tr[t + 2])];
+    const auto &c = P->C.blocks[P->C.find(tr[t], tr[t + 2])];
+    cudaError_t e = P->dtype == BS_F64
+                        ? launch_control_fp64((const double *)A, (const double *)B, (double *)C, a.offset, a.ld,
+                                              b.offset, b.ld, c.offset, c.ld, a.rows, b.cols, a.cols, s)
+                        : launch_control_bf16((const uint16_t *)A, (const uint16_t *)B, (float *)C, a.offset, a.ld,
+                                              b.offset, b.ld, c.offset, c.ld, a.rows, b.cols, a.cols, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return BS_OK;
+}
+
+bs_status bs_plan_last_device_error(bs_plan *P, void *stream) {
+  if (!P || P->opts.host_only) return BS_ERR_INVALID_ARG;
+  BS_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  int32_t v = 0;
+  BS_CUDA(cudaMemcpy(&v, P->d_status, sizeof v, cudaMemcpyDeviceToHost));
+  if (v != 0) {
+    BS_CUDA(cudaMemset(P->d_status, 0, sizeof v));
+    // a kernel that stopped early may leave the work counters set
+    BS_CUDA(cudaMemset(P->d_counter, 0, 16));
+  }
+  if (v == DS_OK) return BS_OK;
+  if (v == DS_TIMEOUT) return BS_ERR_TIMEOUT;
+  return BS_ERR_DEVICE;
+}
+
+void bs_plan_destroy(bs_plan *P) {
+  if (!P) return;
+  free_device(P);
+  delete P;
+}
+
+}  // extern "C"

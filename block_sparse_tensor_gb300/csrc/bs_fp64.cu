@@ -1,0 +1,296 @@
+// FP64 persistent grouped GEMM, gather ("pack") kernel, zero fill, and the
+// one-launch-per-triple control kernel.
+//
+// The grouped kernel runs the whole task list of a plan in one launch
+// (uni20 design note "block coalescing", Summary: fewer, larger kernels;
+// the inferensys glossary "Sparse Operator Fusion": persistent thread blocks
+// and warp-level gather-compute-scatter).  Resident CTAs take tasks from a
+// global counter in longest-first order:
+//   - TILE: the CTA computes a tm x tn tile of one group.  Each K chunk of the
+//     group's concatenated inner axis is staged in shared memory through
+//     per-row and per-k address tables, so inner blocks of any size and any
+//     number of views cost no padding flops.  Outputs are spread one per
+//     thread slot, so a tile of any shape keeps the FP64 lanes busy.
+//   - TAIL: up to eight tiny groups (at most 64 outputs each), one warp per
+//     group, accumulating in registers straight from the L1-cached operands.
+// Stores are plain for contraction-axis groups (each C block has one writer)
+// and atomic adds for free-axis groups (several k add into one C block).
+#include "bs_host.h"
+
+namespace bs {
+
+namespace {
+
+__device__ __forceinline__ int find_rseg(const RowSeg *rs, int n, int r) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (rs[mid].r0 <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int find_kseg(const KSeg *ks, int n, int k) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ks[mid].k0 <= k) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct TileSmem {
+  double As[kKC][kTileMaxDim + 1];   // A chunk, inner index major: As[kk][row]
+  double Bs[kKC][kTileMaxDim + 1];   // B chunk: Bs[kk][col]
+  int64_t rowA[kTileMaxDim];
+  int64_t rowC[kTileMaxDim];
+  int64_t rowL[kTileMaxDim];
+  int64_t kA[kKC];
+  int64_t kL[kKC];
+  int64_t kB[kKC];
+  int task;
+};
+
+__device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
+  const int tid = threadIdx.x;
+  const Group G = p.groups[T.g];
+  const RowSeg *rs = p.rsegs + G.rseg_begin;
+  const KSeg *ks = p.ksegs + G.kseg_begin;
+  const int tm = T.tm, tn = T.tn;
+  for (int r = tid; r < tm; r += kThreads) {
+    const int gr = T.m0 + r;
+    const RowSeg s = rs[find_rseg(rs, G.rseg_count, gr)];
+    const int64_t lr = gr - s.r0;
+    sm.rowA[r] = s.ra + lr * s.lda;
+    sm.rowL[r] = s.rl ? lr : 0;
+    sm.rowC[r] = s.rc + lr * s.ldc;
+  }
+  // this thread's outputs: e = tid + kThreads * u
+  const int ne = tm * tn;
+  int orow[kElemsPerThread], ocol[kElemsPerThread];
+  double acc[kElemsPerThread];
+#pragma unroll
+  for (int u = 0; u < kElemsPerThread; ++u) {
+    const int e = tid + kThreads * u;
+    orow[u] = e < ne ? e / tn : -1;
+    ocol[u] = e < ne ? e - (e / tn) * tn : 0;
+    acc[u] = 0.0;
+  }
+  const bool active = tid < ne;   // warps past the tile's outputs only help load
+  for (int kc0 = 0; kc0 < G.k; kc0 += kKC) {
+    const int kn = min(kKC, G.k - kc0);
+    if (tid < kn) {
+      const int kk = kc0 + tid;
+      const KSeg s = ks[find_kseg(ks, G.kseg_count, kk)];
+      const int64_t pp = kk - s.k0;
+      sm.kA[tid] = s.ka + pp;
+      sm.kL[tid] = s.kl;
+      sm.kB[tid] = s.kb + pp * s.ldb + T.n0;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < tm * kn; idx += kThreads) {
+      const int r = idx / kn, kk = idx - r * kn;
+      sm.As[kk][r] = __ldg(p.A + sm.rowA[r] + sm.kA[kk] + sm.rowL[r] * sm.kL[kk]);
+    }
+    for (int idx = tid; idx < kn * tn; idx += kThreads) {
+      const int kk = idx / tn, c = idx - kk * tn;
+      sm.Bs[kk][c] = __ldg(p.B + sm.kB[kk] + c);
+    }
+    __syncthreads();
+    if (active) {
+      for (int kk = 0; kk < kn; ++kk) {
+#pragma unroll
+        for (int u = 0; u < kElemsPerThread; ++u)
+          if (orow[u] >= 0) acc[u] = fma(sm.As[kk][orow[u]], sm.Bs[kk][ocol[u]], acc[u]);
+      }
+    }
+    __syncthreads();
+  }
+  const bool atomic = (G.flags & GF_ATOMIC) != 0;
+#pragma unroll
+  for (int u = 0; u < kElemsPerThread; ++u) {
+    if (orow[u] < 0) continue;
+    double *dst = p.C + sm.rowC[orow[u]] + T.n0 + ocol[u];
+    if (atomic) atomicAdd(dst, acc[u]);
+    else *dst = acc[u];
+  }
+}
+
+__device__ void run_tail(const Fp64Params &p, const Task &T) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= T.m0) return;
+  const Group G = p.groups[p.tail_groups[T.g + warp]];
+  const RowSeg *rs = p.rsegs + G.rseg_begin;
+  const KSeg *ks = p.ksegs + G.kseg_begin;
+  const int ne = G.m * G.n;
+  // two outputs per lane (tiny groups hold at most 64)
+  int64_t ra[2], rl[2], rc[2];
+  int col[2];
+  bool ok[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int e = lane + 32 * u;
+    ok[u] = e < ne;
+    const int r = ok[u] ? e / G.n : 0;
+    col[u] = ok[u] ? e - r * G.n : 0;
+    const RowSeg s = rs[find_rseg(rs, G.rseg_count, r)];
+    const int64_t lr = r - s.r0;
+    ra[u] = s.ra + lr * s.lda;
+    rl[u] = s.rl ? lr : 0;
+    rc[u] = s.rc + lr * s.ldc;
+  }
+  double acc0 = 0.0, acc1 = 0.0;
+  for (int si = 0; si < G.kseg_count; ++si) {
+    const KSeg s = ks[si];
+    const double *a0 = p.A + ra[0] + s.ka + rl[0] * s.kl;
+    const double *a1 = p.A + ra[1] + s.ka + rl[1] * s.kl;
+    const double *b0 = p.B + s.kb + col[0];
+    const double *b1 = p.B + s.kb + col[1];
+    const int64_t ldb = s.ldb;
+    if (ok[1]) {
+#pragma unroll 4
+      for (int q = 0; q < s.klen; ++q) {
+        acc0 = fma(__ldg(a0 + q), __ldg(b0 + q * ldb), acc0);
+        acc1 = fma(__ldg(a1 + q), __ldg(b1 + q * ldb), acc1);
+      }
+    } else if (ok[0]) {
+#pragma unroll 4
+      for (int q = 0; q < s.klen; ++q) acc0 = fma(__ldg(a0 + q), __ldg(b0 + q * ldb), acc0);
+    }
+  }
+  const bool atomic = (G.flags & GF_ATOMIC) != 0;
+  if (ok[0]) {
+    double *d = p.C + rc[0] + col[0];
+    if (atomic) atomicAdd(d, acc0);
+    else *d = acc0;
+  }
+  if (ok[1]) {
+    double *d = p.C + rc[1] + col[1];
+    if (atomic) atomicAdd(d, acc1);
+    else *d = acc1;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 3) fp64_grouped_kernel(Fp64Params p) {
+  __shared__ TileSmem sm;
+  for (;;) {
+    if (threadIdx.x == 0) sm.task = (int)atomicAdd(&p.counter[0], 1u);
+    __syncthreads();
+    const int t = sm.task;
+    __syncthreads();
+    if (t >= p.ntasks) break;
+    const Task T = p.tasks[t];
+    if (T.kind == TK_TILE) run_tile(p, T, sm);
+    else run_tail(p, T);
+  }
+  // The last CTA to leave returns both counters to zero for the next launch.
+  // Every CTA has taken its final task index before it counts itself out.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(&p.counter[1], 1u);
+    if (prev == gridDim.x - 1) {
+      atomicExch(&p.counter[0], 0u);
+      atomicExch(&p.counter[1], 0u);
+    }
+  }
+}
+
+template <class T>
+__global__ void pack_kernel(PackParams a, PackParams b, int32_t ntotal) {
+  for (int c = blockIdx.x; c < ntotal; c += gridDim.x) {
+    const bool is_a = c < a.ncopies;
+    const PackParams &pp = is_a ? a : b;
+    const PackCopy cp = pp.copies[c];
+    const T *src = (const T *)pp.src + cp.src;
+    T *dst = (T *)pp.dst + cp.dst;
+    const int n = cp.rows * cp.cols;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      const int r = e / cp.cols, q = e - r * cp.cols;
+      dst[(int64_t)r * cp.dst_ld + q] = src[(int64_t)r * cp.src_ld + q];
+    }
+  }
+}
+
+template <class T>
+__global__ void zero_kernel(T *C, const ZeroBlock *blocks, int nblocks) {
+  for (int bi = blockIdx.x; bi < nblocks; bi += gridDim.x) {
+    const ZeroBlock z = blocks[bi];
+    const int n = z.rows * z.cols;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      const int r = e / z.cols, q = e - r * z.cols;
+      C[z.off + (int64_t)r * z.ld + q] = T(0);
+    }
+  }
+}
+
+__global__ void control_fp64_kernel(const double *A, const double *B, double *C, int64_t a_off, int64_t lda,
+                                    int64_t b_off, int64_t ldb, int64_t c_off, int64_t ldc, int m, int n, int k) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= m * n) return;
+  const int r = e / n, c = e - r * n;
+  double acc = 0.0;
+  for (int q = 0; q < k; ++q) acc = fma(A[a_off + r * lda + q], B[b_off + q * ldb + c], acc);
+  C[c_off + r * ldc + c] += acc;
+}
+
+__global__ void control_bf16_kernel(const uint16_t *A, const uint16_t *B, float *C, int64_t a_off, int64_t lda,
+                                    int64_t b_off, int64_t ldb, int64_t c_off, int64_t ldc, int m, int n, int k) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= m * n) return;
+  const int r = e / n, c = e - r * n;
+  float acc = 0.f;
+  for (int q = 0; q < k; ++q) {
+    const float a = __uint_as_float((uint32_t)A[a_off + r * lda + q] << 16);
+    const float b = __uint_as_float((uint32_t)B[b_off + q * ldb + c] << 16);
+    acc = fmaf(a, b, acc);
+  }
+  C[c_off + r * ldc + c] += acc;
+}
+
+}  // namespace
+
+cudaError_t launch_fp64_grouped(const Fp64Params &p, int grid, cudaStream_t s) {
+  fp64_grouped_kernel<<<grid, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+int fp64_max_ctas_per_sm() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp64_grouped_kernel, kThreads, 0) != cudaSuccess) return 1;
+  return n;
+}
+
+cudaError_t launch_pack2(const PackParams &a, const PackParams &b, int32_t ntotal, int grid, cudaStream_t s) {
+  if (ntotal <= 0) return cudaSuccess;
+  grid = grid < ntotal ? grid : ntotal;
+  if (a.elem_bytes == 8) pack_kernel<double><<<grid, 256, 0, s>>>(a, b, ntotal);
+  else pack_kernel<uint16_t><<<grid, 256, 0, s>>>(a, b, ntotal);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero(void *C, int elem_bytes, const ZeroBlock *blocks, int nblocks, int grid, cudaStream_t s) {
+  if (nblocks <= 0) return cudaSuccess;
+  grid = grid < nblocks ? grid : nblocks;
+  if (elem_bytes == 8) zero_kernel<double><<<grid, 256, 0, s>>>((double *)C, blocks, nblocks);
+  else zero_kernel<float><<<grid, 256, 0, s>>>((float *)C, blocks, nblocks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_control_fp64(const double *A, const double *B, double *C, int64_t a_off, int64_t lda, int64_t b_off,
+                                int64_t ldb, int64_t c_off, int64_t ldc, int m, int n, int k, cudaStream_t s) {
+  const int e = m * n;
+  control_fp64_kernel<<<(e + 127) / 128, 128, 0, s>>>(A, B, C, a_off, lda, b_off, ldb, c_off, ldc, m, n, k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_control_bf16(const uint16_t *A, const uint16_t *B, float *C, int64_t a_off, int64_t lda,
+                                int64_t b_off, int64_t ldb, int64_t c_off, int64_t ldc, int m, int n, int k,
+                                cudaStream_t s) {
+  const int e = m * n;
+  control_bf16_kernel<<<(e + 127) / 128, 128, 0, s>>>(A, B, C, a_off, lda, b_off, ldb, c_off, ldc, m, n, k);
+  return cudaGetLastError();
+}
+
+}  // namespace bs

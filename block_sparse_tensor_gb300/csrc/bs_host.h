@@ -1,0 +1,81 @@
+// Host-side objects behind the opaque handles of bs.h.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/bs.h"
+#include "bs_internal.h"
+
+namespace bs {
+
+struct AxisCopy {
+  int32_t n = 0;
+  std::vector<int32_t> q;
+  std::vector<uint8_t> p;   // empty when the axis has no parity
+  std::vector<int32_t> d;
+  bool same_as(const AxisCopy &o) const { return n == o.n && q == o.q && p == o.p && d == o.d; }
+};
+
+// Populated set given as rows of sorted column indices (CSR).
+struct Sparsity {
+  std::vector<int64_t> ptr;   // n_rows + 1
+  std::vector<int32_t> cols;  // ascending within a row
+};
+
+}  // namespace bs
+
+struct bs_layout {
+  bs::AxisCopy rows, cols;
+  uint32_t flags = 0;
+  int32_t elem_bytes = 8;
+  int64_t nelems = 0;
+  std::vector<bs_block_info> blocks;   // storage order
+  // CSR by row sector over blocks: row_ptr[r] .. row_ptr[r+1] index row_blk,
+  // listing the row's blocks in storage order; csc likewise by column.
+  std::vector<int64_t> row_ptr, col_ptr;
+  std::vector<int32_t> row_blk, col_blk;
+  // dense (row, col) -> block index when the grid is small enough, else empty
+  std::vector<int32_t> grid;
+  int32_t find(int32_t r, int32_t c) const;
+};
+
+namespace bs {
+
+bs_status build_layout(const AxisCopy &rows, const AxisCopy &cols, const Sparsity &sp, uint32_t flags,
+                       int32_t elem_bytes, bs_layout *out);
+bs_status copy_axis(const bs_axis_desc *d, AxisCopy *out);
+Sparsity rule_sparsity(const AxisCopy &r, const AxisCopy &c, const bs_rule &rule);
+
+// Launchers (bs_fp64.cu, bs_bf16.cu).
+cudaError_t launch_fp64_grouped(const Fp64Params &p, int grid, cudaStream_t s);
+cudaError_t launch_pack2(const PackParams &a, const PackParams &b, int32_t ntotal, int grid, cudaStream_t s);
+cudaError_t launch_zero(void *C, int elem_bytes, const ZeroBlock *blocks, int nblocks, int grid,
+                        cudaStream_t s);
+cudaError_t launch_control_fp64(const double *A, const double *B, double *C, int64_t a_off, int64_t lda,
+                                int64_t b_off, int64_t ldb, int64_t c_off, int64_t ldc, int m, int n, int k,
+                                cudaStream_t s);
+cudaError_t launch_control_bf16(const uint16_t *A, const uint16_t *B, float *C, int64_t a_off, int64_t lda,
+                                int64_t b_off, int64_t ldb, int64_t c_off, int64_t ldc, int m, int n, int k,
+                                cudaStream_t s);
+int fp64_max_ctas_per_sm();
+
+struct Bf16Params {
+  const void *maps;        // CUtensorMap array in device memory (64-byte aligned)
+  const Bf16Task *tasks;
+  const Bf16Pair *pairs;
+  float *C;
+  int32_t ntasks;
+  int32_t pad_;
+  int32_t *status;
+  uint32_t *counter;
+  uint64_t timeout_ns;
+  int32_t debug_flags;
+  int32_t pad2_;
+};
+cudaError_t launch_bf16_grouped(const Bf16Params &p, int grid, cudaStream_t s);
+size_t bf16_smem_bytes();
+
+}  // namespace bs

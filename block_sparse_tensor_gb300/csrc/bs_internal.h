@@ -1,0 +1,147 @@
+// Internal structures shared by the host planner and the device kernels.
+//
+// A coalesced group is one dense GEMM, C_g[M x N] (+)= A_g[M x K] B_g[K x N],
+// whose operands are unions of block views ("Expressed as strided views over
+// shared storage", uni20 design note "block coalescing").  Every group is
+// described by two segment lists and one addressing rule:
+//
+//   A(r, kk) = A[ RA(r) + KA(kk) + RL(r) * KL(kk) ]
+//   B(kk, c) = B[ KB(kk) + c ]
+//   C(r, c)  = C[ RC(r) + c ]
+//
+// Row segment t covers rows r0 .. r0+rows-1 of the group:
+//   RA(r) = ra + (r - r0) * lda,  RL(r) = rl ? (r - r0) : 0,  RC(r) = rc + (r - r0) * ldc.
+// Inner segment s covers k0 .. k0+klen-1 of the group's concatenated K:
+//   KA(kk) = ka + (kk - k0),  KL(kk) = kl,  KB(kk) = kb + (kk - k0) * ldb.
+//
+// Contraction-axis group (fixed i, j; K concatenated): one row segment
+// {ra 0, lda 0, rl 1, rc c_off, ldc} and one inner segment per run of
+// adjacent blocks {ka a_off, kl lda, kb b_off, ldb}.
+// Free-axis group (fixed k, j; rows stacked): one row segment per run of
+// stacked A blocks {ra a_off, lda, rl 0, rc c_off(i, j), ldc} and one inner
+// segment {ka 0, kl 0, kb b_off, ldb}; its stores are atomic adds.
+#pragma once
+#include <stdint.h>
+
+namespace bs {
+
+struct RowSeg {
+  int64_t ra;
+  int64_t lda;
+  int64_t rc;
+  int64_t ldc;
+  int32_t r0;
+  int32_t rows;
+  int32_t rl;
+  int32_t pad_;
+};
+
+struct KSeg {
+  int64_t ka;
+  int64_t kl;
+  int64_t kb;
+  int64_t ldb;
+  int32_t k0;
+  int32_t klen;
+};
+
+enum GroupFlags : int32_t { GF_ATOMIC = 1 };
+
+struct Group {
+  int32_t m, n, k;
+  int32_t flags;
+  int32_t rseg_begin, rseg_count;
+  int32_t kseg_begin, kseg_count;
+};
+
+enum TaskKind : int32_t { TK_TILE = 0, TK_TAIL = 1 };
+
+// TK_TILE: one CTA computes rows m0 .. m0+tm-1, columns n0 .. n0+tn-1 of group `g`.
+// TK_TAIL: one CTA runs up to kTailPerTask tiny groups, one warp each; their
+//          ids are tail_groups[first .. first+count-1].
+struct Task {
+  int32_t kind;
+  int32_t g;       // group (TILE) or first index into tail_groups (TAIL)
+  int32_t m0;      // (TILE) or count (TAIL)
+  int32_t n0;
+  int32_t tm;
+  int32_t tn;
+};
+
+constexpr int kThreads = 256;          // threads of the FP64 grouped kernel
+constexpr int kElemsPerThread = 4;     // tile outputs per thread
+constexpr int kTileMaxElems = kThreads * kElemsPerThread;
+constexpr int kTileMaxDim = 128;       // bound on tm and tn
+constexpr int kKC = 16;                // inner chunk per shared-memory stage
+constexpr int kTailPerTask = kThreads / 32;
+constexpr int kTailMaxElems = 64;      // a group this small runs on one warp
+
+// One block copy of the gather ("pack") kernel.
+struct PackCopy {
+  int64_t src;
+  int64_t src_ld;
+  int64_t dst;
+  int64_t dst_ld;
+  int32_t rows;
+  int32_t cols;
+};
+
+// One C block for the zero fill that precedes atomic scatter.
+struct ZeroBlock {
+  int64_t off;
+  int64_t ld;
+  int32_t rows;
+  int32_t cols;
+};
+
+// Device status word values (first int of the status buffer).
+enum DeviceStatus : int32_t { DS_OK = 0, DS_TIMEOUT = 1, DS_BOUNDS = 2 };
+
+struct Fp64Params {
+  const double *A;
+  const double *B;
+  double *C;
+  const Task *tasks;
+  const Group *groups;
+  const RowSeg *rsegs;
+  const KSeg *ksegs;
+  const int32_t *tail_groups;
+  int32_t ntasks;
+  int32_t pad_;
+  uint32_t *counter;   // [0] next task, [1] CTAs finished; both return to 0 at exit
+  int32_t *status;
+};
+
+struct PackParams {
+  const void *src;
+  void *dst;
+  const PackCopy *copies;
+  int32_t ncopies;
+  int32_t elem_bytes;
+};
+
+// ---- BF16 tensor-core path ------------------------------------------------
+// One task = a 128 x BN tile of a contraction-axis group; its K loop walks the
+// group's block pairs, each with its own tensor maps (zero fill past the
+// block edge keeps ragged K exact).
+struct Bf16Pair {
+  int32_t map_a;   // index of the A tensor map (rows of the group x d_k)
+  int32_t map_b;   // index of the B tensor map (d_k x cols of the group)
+  int32_t klen;    // d_k
+  int32_t pad_;
+};
+
+struct Bf16Task {
+  int32_t pair_begin;
+  int32_t pair_count;
+  int32_t m0;        // first row of the tile inside the group
+  int32_t n0;        // first column of the tile inside the group
+  int32_t m;         // rows of the group
+  int32_t n;         // columns of the group
+  int32_t bn;        // UMMA N of the tile (multiple of 16, <= 256)
+  int32_t pad_;
+  int64_t c_off;     // C offset of the group's (0, 0) element
+  int64_t ldc;
+};
+
+}  // namespace bs

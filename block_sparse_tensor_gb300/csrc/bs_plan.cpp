@@ -1,0 +1,370 @@
+// Structural product, coalescing planner and cost model (host).
+//
+// Follows the uni20 design note "block coalescing":
+//   - "Why single-axis coalescing is hole-free": groups are taken along one
+//     axis.  Contraction-axis group = one C block (i, j) with its inner blocks
+//     k concatenated into one wider-K GEMM; free-axis group = one (k, j) with
+//     the A blocks A[., k] stacked into one taller GEMM.  Either choice lists
+//     only populated blocks, so no group holds a structural zero.
+//   - "Interleaved vs contiguous": adjacent blocks whose strides agree merge
+//     into one wider view (zero copy); otherwise the group walks several views
+//     or the operand is gathered into a panel workspace, whichever the cost
+//     model prefers ("pack cost vs launch savings").
+//   - "Two coalescing modes" / "The crossover decides whether to coalesce": a
+//     single-axis group carries no wasted flops, so the only trade is per-task
+//     and per-segment overhead against gather bytes.
+//   - "Coalescing is a plan-time transform": everything here runs once per plan.
+//   - "Interleaved" LocalSpace keys: row sectors whose groups have the same
+//     inner blocks and whose A and C rows continue each other with one stride
+//     are stacked into one taller group (merge_rows).
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <numeric>
+
+#include "bs_plan.h"
+
+namespace bs {
+
+namespace {
+
+struct Builder {
+  GroupSet gs;
+  void add_triple(int32_t i, int32_t k, int32_t j) {
+    gs.triples.push_back(i);
+    gs.triples.push_back(k);
+    gs.triples.push_back(j);
+  }
+  void close_group() { gs.tptr.push_back((int64_t)gs.triples.size() / 3); }
+};
+
+struct Entry {
+  int32_t k, blk_a, blk_b;
+};
+
+}  // namespace
+
+// One group per C block: the inner blocks in A's storage order, merged into
+// runs where both the A view and the B view continue with the same stride.
+GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C, bool merge_rows,
+                                 bool atomic) {
+  Builder bd;
+  GroupSet &gs = bd.gs;
+  gs.tptr.push_back(0);
+  const int32_t ni = A.rows.n, nj = B.cols.n;
+  std::vector<std::vector<Entry>> bucket(nj);
+  std::vector<int32_t> touched;
+  // for row merging: the last group per column, its last row sector and entries
+  std::vector<int32_t> last_group(nj, -1), last_row(nj, -1);
+  std::vector<std::vector<Entry>> last_entries(merge_rows ? nj : 0);
+  for (int32_t i = 0; i < ni; ++i) {
+    touched.clear();
+    for (int64_t t = A.row_ptr[i]; t < A.row_ptr[i + 1]; ++t) {
+      const int32_t ba = A.row_blk[t];
+      const int32_t k = A.blocks[ba].col;
+      for (int64_t u = B.row_ptr[k]; u < B.row_ptr[k + 1]; ++u) {
+        const int32_t bb = B.row_blk[u];
+        const int32_t j = B.blocks[bb].col;
+        if (bucket[j].empty()) touched.push_back(j);
+        bucket[j].push_back({k, ba, bb});
+      }
+    }
+    std::sort(touched.begin(), touched.end());
+    for (int32_t j : touched) {
+      auto &ent = bucket[j];
+      const int32_t cb = C.find(i, j);
+      const bs_block_info &cbi = C.blocks[cb];
+      bool merged = false;
+      if (merge_rows && last_group[j] >= 0 && last_row[j] == i - 1 && last_entries[j].size() == ent.size()) {
+        Group &g = gs.groups[last_group[j]];
+        const RowSeg &rs = gs.rsegs[g.rseg_begin];
+        bool ok = g.rseg_count == 1 && (g.flags & GF_ATOMIC) == (atomic ? GF_ATOMIC : 0) && rs.ldc == cbi.ld &&
+                  cbi.offset == rs.rc + (int64_t)g.m * rs.ldc;
+        for (size_t e = 0; ok && e < ent.size(); ++e) {
+          const auto &a0 = A.blocks[last_entries[j][e].blk_a];
+          const auto &a1 = A.blocks[ent[e].blk_a];
+          // same inner block, same B block, A rows continuing the group's rows
+          ok = last_entries[j][e].k == ent[e].k && last_entries[j][e].blk_b == ent[e].blk_b && a1.ld == a0.ld &&
+               a1.offset == a0.offset + (int64_t)g.m * a0.ld;
+        }
+        if (ok) {
+          // last_entries keeps the group's first row sector, which the offsets are relative to
+          g.m += A.rows.d[i];
+          gs.rsegs[g.rseg_begin].rows += A.rows.d[i];
+          // triples of the merged row: insert before the sentinel of this group
+          // (groups are closed in order, so append to the group's range only if it is the last)
+          merged = true;
+          last_row[j] = i;
+          // record the triples of row i for this group
+          for (const auto &e : ent) gs.extra_triples.push_back({last_group[j], i, e.k, j});
+        }
+      }
+      if (!merged) {
+        Group g{};
+        g.n = B.cols.d[j];
+        g.m = A.rows.d[i];
+        g.flags = atomic ? GF_ATOMIC : 0;
+        g.rseg_begin = (int32_t)gs.rsegs.size();
+        g.rseg_count = 1;
+        RowSeg rs{};
+        rs.ra = 0;
+        rs.lda = 0;
+        rs.rc = cbi.offset;
+        rs.ldc = cbi.ld;
+        rs.r0 = 0;
+        rs.rows = g.m;
+        rs.rl = 1;
+        gs.rsegs.push_back(rs);
+        g.kseg_begin = (int32_t)gs.ksegs.size();
+        int32_t kpos = 0;
+        for (const auto &e : ent) {
+          const auto &a = A.blocks[e.blk_a];
+          const auto &b = B.blocks[e.blk_b];
+          const int32_t dk = A.cols.d[e.k];
+          bool join = false;
+          if ((int32_t)gs.ksegs.size() > g.kseg_begin) {
+            KSeg &s = gs.ksegs.back();
+            join = a.ld == s.kl && a.offset == s.ka + s.klen && b.ld == s.ldb && b.offset == s.kb + (int64_t)s.klen * s.ldb;
+            if (join) s.klen += dk;
+          }
+          if (!join) {
+            KSeg s{};
+            s.ka = a.offset;
+            s.kl = a.ld;
+            s.kb = b.offset;
+            s.ldb = b.ld;
+            s.k0 = kpos;
+            s.klen = dk;
+            gs.ksegs.push_back(s);
+          }
+          kpos += dk;
+          bd.add_triple(i, e.k, j);
+        }
+        g.k = kpos;
+        g.kseg_count = (int32_t)gs.ksegs.size() - g.kseg_begin;
+        gs.groups.push_back(g);
+        bd.close_group();
+        if (merge_rows) {
+          last_group[j] = (int32_t)gs.groups.size() - 1;
+          last_row[j] = i;
+          last_entries[j] = ent;
+        }
+      }
+      ent.clear();
+    }
+  }
+  return gs;
+}
+
+// One group per (k, j): the A blocks of inner sector k stacked in A's storage
+// order; runs whose A rows and C rows continue with one stride share a row
+// segment.  Several groups add into the same C block, so stores are atomic.
+GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C) {
+  Builder bd;
+  GroupSet &gs = bd.gs;
+  gs.tptr.push_back(0);
+  const int32_t nk = A.cols.n;
+  for (int32_t k = 0; k < nk; ++k) {
+    if (A.col_ptr[k] == A.col_ptr[k + 1]) continue;
+    for (int64_t u = B.row_ptr[k]; u < B.row_ptr[k + 1]; ++u) {
+      const auto &b = B.blocks[B.row_blk[u]];
+      const int32_t j = b.col;
+      Group g{};
+      g.n = B.cols.d[j];
+      g.k = A.cols.d[k];
+      g.flags = GF_ATOMIC;
+      g.rseg_begin = (int32_t)gs.rsegs.size();
+      int32_t r = 0;
+      for (int64_t t = A.col_ptr[k]; t < A.col_ptr[k + 1]; ++t) {
+        const auto &a = A.blocks[A.col_blk[t]];
+        const int32_t i = a.row;
+        const auto &c = C.blocks[C.find(i, j)];
+        bool join = false;
+        if ((int32_t)gs.rsegs.size() > g.rseg_begin) {
+          RowSeg &s = gs.rsegs.back();
+          join = a.ld == s.lda && a.offset == s.ra + (int64_t)s.rows * s.lda && c.ld == s.ldc &&
+                 c.offset == s.rc + (int64_t)s.rows * s.ldc;
+          if (join) s.rows += a.rows;
+        }
+        if (!join) {
+          RowSeg s{};
+          s.ra = a.offset;
+          s.lda = a.ld;
+          s.rc = c.offset;
+          s.ldc = c.ld;
+          s.r0 = r;
+          s.rows = a.rows;
+          s.rl = 0;
+          gs.rsegs.push_back(s);
+        }
+        r += a.rows;
+        bd.add_triple(i, k, j);
+      }
+      g.m = r;
+      g.rseg_count = (int32_t)gs.rsegs.size() - g.rseg_begin;
+      g.kseg_begin = (int32_t)gs.ksegs.size();
+      g.kseg_count = 1;
+      KSeg s{};
+      s.ka = 0;
+      s.kl = 0;
+      s.kb = b.offset;
+      s.ldb = b.ld;
+      s.k0 = 0;
+      s.klen = g.k;
+      gs.ksegs.push_back(s);
+      gs.groups.push_back(g);
+      bd.close_group();
+    }
+  }
+  return gs;
+}
+
+// No coalescing: one group per populated triple, scattered atomically.
+GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C) {
+  Builder bd;
+  GroupSet &gs = bd.gs;
+  gs.tptr.push_back(0);
+  for (int32_t i = 0; i < A.rows.n; ++i)
+    for (int64_t t = A.row_ptr[i]; t < A.row_ptr[i + 1]; ++t) {
+      const auto &a = A.blocks[A.row_blk[t]];
+      const int32_t k = a.col;
+      for (int64_t u = B.row_ptr[k]; u < B.row_ptr[k + 1]; ++u) {
+        const auto &b = B.blocks[B.row_blk[u]];
+        const auto &c = C.blocks[C.find(i, b.col)];
+        Group g{};
+        g.m = a.rows;
+        g.n = b.cols;
+        g.k = a.cols;
+        g.flags = GF_ATOMIC;
+        g.rseg_begin = (int32_t)gs.rsegs.size();
+        g.rseg_count = 1;
+        RowSeg rs{};
+        rs.rc = c.offset;
+        rs.ldc = c.ld;
+        rs.rows = g.m;
+        rs.rl = 1;
+        gs.rsegs.push_back(rs);
+        g.kseg_begin = (int32_t)gs.ksegs.size();
+        g.kseg_count = 1;
+        KSeg s{};
+        s.ka = a.offset;
+        s.kl = a.ld;
+        s.kb = b.offset;
+        s.ldb = b.ld;
+        s.klen = g.k;
+        gs.ksegs.push_back(s);
+        gs.groups.push_back(g);
+        bd.add_triple(i, k, b.col);
+        bd.close_group();
+      }
+    }
+  return gs;
+}
+
+// Triples of every group, group by group, with merged rows folded in.
+void group_triples(const GroupSet &gs, std::vector<int64_t> *ptr, std::vector<int32_t> *out) {
+  const size_t ng = gs.groups.size();
+  std::vector<std::vector<int32_t>> extra(ng);
+  for (const auto &e : gs.extra_triples) {
+    extra[e[0]].push_back(e[1]);
+    extra[e[0]].push_back(e[2]);
+    extra[e[0]].push_back(e[3]);
+  }
+  ptr->assign(ng + 1, 0);
+  out->clear();
+  for (size_t g = 0; g < ng; ++g) {
+    out->insert(out->end(), gs.triples.begin() + 3 * gs.tptr[g], gs.triples.begin() + 3 * gs.tptr[g + 1]);
+    out->insert(out->end(), extra[g].begin(), extra[g].end());
+    (*ptr)[g + 1] = (int64_t)out->size() / 3;
+  }
+}
+
+// ---- FP64 tiling -----------------------------------------------------------
+
+static void tile_shape(int32_t m, int32_t n, int32_t *tm, int32_t *tn) {
+  // Outputs are spread one per thread-slot, so any tm x tn <= kTileMaxElems keeps
+  // every lane busy; the shape only has to follow the group's aspect ratio.
+  if (n <= 8) {
+    *tn = n;
+    *tm = std::min(m, std::min(kTileMaxDim, kTileMaxElems / n));
+  } else if (m <= 8) {
+    *tm = m;
+    *tn = std::min(n, std::min(kTileMaxDim, kTileMaxElems / m));
+  } else {
+    *tn = std::min(n, 32);
+    *tm = std::min(m, std::min(kTileMaxDim, kTileMaxElems / *tn));
+  }
+}
+
+static inline int64_t lanes(int64_t e) { return (e + 31) / 32 * 32; }
+
+void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
+  ts->tasks.clear();
+  ts->tail_groups.clear();
+  std::vector<std::pair<double, Task>> costed;
+  std::vector<int32_t> tails;
+  double exec = 0;
+  for (int32_t g = 0; g < (int32_t)gs.groups.size(); ++g) {
+    const Group &G = gs.groups[g];
+    const int64_t e = (int64_t)G.m * G.n;
+    if (e <= kTailMaxElems) {
+      tails.push_back(g);
+      exec += 2.0 * lanes(e) * G.k;
+      continue;
+    }
+    int32_t tm, tn;
+    tile_shape(G.m, G.n, &tm, &tn);
+    for (int32_t m0 = 0; m0 < G.m; m0 += tm)
+      for (int32_t n0 = 0; n0 < G.n; n0 += tn) {
+        Task t{};
+        t.kind = TK_TILE;
+        t.g = g;
+        t.m0 = m0;
+        t.n0 = n0;
+        t.tm = std::min(tm, G.m - m0);
+        t.tn = std::min(tn, G.n - n0);
+        const double slots = (double)lanes((int64_t)t.tm * t.tn);
+        exec += 2.0 * slots * G.k;
+        costed.push_back({slots * G.k + pm.task_slots, t});
+      }
+  }
+  // tiny groups: longest K first, bundled kTailPerTask at a time so the warps
+  // of one bundle finish together
+  std::stable_sort(tails.begin(), tails.end(),
+                   [&](int32_t a, int32_t b) { return gs.groups[a].k > gs.groups[b].k; });
+  ts->tail_groups = tails;
+  for (size_t f = 0; f < tails.size(); f += kTailPerTask) {
+    Task t{};
+    t.kind = TK_TAIL;
+    t.g = (int32_t)f;
+    t.m0 = (int32_t)std::min<size_t>(kTailPerTask, tails.size() - f);
+    double c = 0;
+    for (int32_t u = 0; u < t.m0; ++u) {
+      const Group &G = gs.groups[tails[f + u]];
+      c = std::max(c, (double)lanes((int64_t)G.m * G.n) * G.k);
+    }
+    costed.push_back({c * kTailPerTask / 2 + pm.task_slots, t});
+  }
+  // longest processing time first for the dynamic scheduler
+  std::stable_sort(costed.begin(), costed.end(),
+                   [](const std::pair<double, Task> &a, const std::pair<double, Task> &b) { return a.first > b.first; });
+  for (auto &c : costed) ts->tasks.push_back(c.second);
+  ts->executed_flops = exec;
+}
+
+double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm, int64_t pack_bytes, int launches) {
+  const double compute = ts.executed_flops / (pm.fp64_gflops * 1e3);
+  int64_t nseg = 0, natomic_elems = 0;
+  for (const auto &g : gs.groups) {
+    nseg += g.kseg_count + g.rseg_count;
+    if (g.flags & GF_ATOMIC) natomic_elems += (int64_t)g.m * g.n;
+  }
+  const double par = std::max(1, pm.parallel_ctas);
+  const double overhead = ((double)ts.tasks.size() * pm.t_task_us + (double)nseg * pm.t_segment_us) / par;
+  const double atomics = pm.atomic_penalty * natomic_elems * 8.0 / (pm.pack_gbs * 1e3);
+  const double pack = pack_bytes > 0 ? 2.0 * pack_bytes / (pm.pack_gbs * 1e3) : 0.0;
+  return compute + overhead + atomics + pack + launches * pm.t_launch_us;
+}
+
+}  // namespace bs

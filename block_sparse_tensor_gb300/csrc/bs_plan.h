@@ -1,0 +1,100 @@
+// Plan objects and planner entry points (host).
+#pragma once
+#include <array>
+#include <vector>
+
+#include "bs_host.h"
+
+namespace bs {
+
+struct GroupSet {
+  std::vector<Group> groups;
+  std::vector<RowSeg> rsegs;
+  std::vector<KSeg> ksegs;
+  // (i, k, j) triples of each group's first row sector: tptr[g] .. tptr[g+1]
+  std::vector<int64_t> tptr;
+  std::vector<int32_t> triples;
+  // triples of row sectors merged into an existing group: {group, i, k, j}
+  std::vector<std::array<int32_t, 4>> extra_triples;
+};
+
+struct TileSet {
+  std::vector<Task> tasks;
+  std::vector<int32_t> tail_groups;
+  double executed_flops = 0;
+};
+
+struct PlanModel {
+  double t_launch_us = 2.0;
+  double t_task_us = 0.4;
+  double t_segment_us = 0.03;
+  double pack_gbs = 3000.0;
+  double fp64_gflops = 1200.0;
+  double atomic_penalty = 0.5;
+  double task_slots = 4096;   // LPT weight of a task's fixed cost, in lane-flop units
+  int parallel_ctas = 456;
+};
+
+GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C, bool merge_rows,
+                                 bool atomic);
+GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C);
+GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C);
+void group_triples(const GroupSet &gs, std::vector<int64_t> *ptr, std::vector<int32_t> *out);
+void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts);
+double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm, int64_t pack_bytes, int launches);
+
+// Host description of one TMA tensor map of the BF16 path (encoded per call
+// with the caller's base pointer, then cached while the pointers stay the same).
+struct MapDesc {
+  int32_t operand;      // 0: A, 1: B
+  int64_t off;          // element offset of the view's first element
+  int64_t inner;        // contiguous extent (elements)
+  int64_t outer;        // rows
+  int64_t ld;           // elements between rows
+  int32_t box_inner;
+  int32_t box_outer;
+};
+
+}  // namespace bs
+
+struct bs_plan {
+  int32_t dtype = BS_F64;
+  bs_plan_options opts{};
+  bs_layout A, B, C;
+  bs_layout A_pk, B_pk;
+  bool pack_a = false, pack_b = false;
+  int32_t axis = BS_AXIS_CONTRACTION;
+  bs::GroupSet gs;
+  bs::TileSet ts;
+  std::vector<bs::PackCopy> pack_copies;   // A copies first, then B copies
+  int32_t pack_copies_a = 0;
+  std::vector<bs::ZeroBlock> zero_blocks;
+  // BF16 path
+  std::vector<bs::Bf16Task> btasks;
+  std::vector<bs::Bf16Pair> bpairs;
+  std::vector<bs::MapDesc> maps;
+  std::vector<unsigned char> map_bytes;   // encoded maps (128 bytes each)
+  const void *maps_a_ptr = nullptr, *maps_b_ptr = nullptr;
+  // device state
+  int device = -1;
+  int sm_count = 0;
+  int grid = 0;
+  void *d_tables = nullptr;
+  size_t tables_bytes = 0;
+  bs::Task *d_tasks = nullptr;
+  bs::Group *d_groups = nullptr;
+  bs::RowSeg *d_rsegs = nullptr;
+  bs::KSeg *d_ksegs = nullptr;
+  int32_t *d_tail = nullptr;
+  bs::PackCopy *d_pack = nullptr;
+  bs::ZeroBlock *d_zero = nullptr;
+  bs::Bf16Task *d_btasks = nullptr;
+  bs::Bf16Pair *d_bpairs = nullptr;
+  void *d_maps = nullptr;
+  void *d_ws_a = nullptr, *d_ws_b = nullptr;
+  uint32_t *d_counter = nullptr;
+  int32_t *d_status = nullptr;
+  // staging for bs_contract_host
+  void *d_host_a = nullptr, *d_host_b = nullptr, *d_host_c = nullptr;
+  bs_plan_stats stats{};
+};

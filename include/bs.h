@@ -1,0 +1,256 @@
+/*
+ * bs.h — C ABI of the coalesced block-sparse contraction library (libbs.so).
+ *
+ * The library computes C[i,j] = sum_k A[i,k] B[k,j] for block-sparse tensors
+ * over symmetry sectors, as described in the uni20 design note "block
+ * coalescing" (uni20-dev.github.io, docs/symmetry/block_coalescing):
+ *   - Summary: every populated (row, inner, column) sector triple is one small
+ *     dense GEMM; the remedy for the many tiny ones is fewer, larger kernels.
+ *   - "Why single-axis coalescing is hole-free": groups are formed along one
+ *     axis only (free axis: stack the A blocks sharing an inner index k into a
+ *     taller GEMM; contraction axis: concatenate the k blocks of one output
+ *     block into a wider-K GEMM), so no group contains a structural zero.
+ *   - "Expressed as strided views over shared storage": each block is an
+ *     (offset, leading dimension) view into one caller-owned buffer, and a
+ *     coalesced operand is a wider view of the same bytes.
+ *   - "Interleaved vs contiguous": a group whose blocks are not stride
+ *     compatible, or not addressable by the tensor-memory copy engine, is
+ *     gathered ("packed") into a workspace; a cost model decides per plan.
+ *   - "Coalescing is a plan-time transform": bs_plan_create builds the groups,
+ *     the task list and the scatter map once; bs_contract only launches.
+ *
+ * Conventions shared by every entry point:
+ *   - Every function returns a bs_status and never throws or aborts.
+ *   - Sizes and offsets are in elements of the buffer's type unless stated.
+ *   - Handles (bs_layout, bs_plan) are opaque and owned by the library; free
+ *     them with the matching *_destroy call.  Destroying NULL is a no-op.
+ *   - Device pointers are CUDA device (or managed) addresses on the device
+ *     that was current when the plan was created.  Streams are cudaStream_t
+ *     passed as void* (NULL = the legacy default stream).
+ */
+#ifndef BS_H
+#define BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bs_status {
+  BS_OK = 0,
+  BS_ERR_INVALID_ARG = 1,     /* NULL handle/pointer, negative size, bad flag, bad option */
+  BS_ERR_SHAPE_MISMATCH = 2,  /* inner axes differ, or a given C layout is not the product */
+  BS_ERR_UNSUPPORTED = 3,     /* dtype or device not supported (needs sm_103 / sm_100 family) */
+  BS_ERR_OOM = 4,             /* host or device allocation failed */
+  BS_ERR_CUDA = 5,            /* a CUDA runtime or driver call failed */
+  BS_ERR_TIMEOUT = 6,         /* a bounded device-side wait ran out (reported by the kernel) */
+  BS_ERR_MISALIGNED = 7,      /* a buffer or view breaks the 16-byte rule of the chosen path */
+  BS_ERR_DEVICE = 8,          /* a device-side consistency check failed */
+  BS_ERR_OVERFLOW = 9         /* an element count or offset does not fit in int64 / int32 */
+} bs_status;
+
+/* One sector axis: n sectors, each with a U(1) charge, an optional Z2 parity
+ * (q_z2 may be NULL) and a dimension >= 1.  Sector identity is its index;
+ * repeated charges are allowed.  Arrays are read during the call only. */
+typedef struct bs_axis_desc {
+  int32_t n;
+  const int32_t *q_u1;
+  const uint8_t *q_z2;
+  const int32_t *dim;
+} bs_axis_desc;
+
+/* Allowed-charge rule of a two-axis tensor: block (r, c) exists iff
+ * dq_min <= q_u1[r] - q_u1[c] <= dq_max and, if z2 != 0, q_z2[r] == q_z2[c]
+ * (both axes must then carry parities). */
+typedef struct bs_rule {
+  int32_t dq_min;
+  int32_t dq_max;
+  int32_t z2;
+} bs_rule;
+
+/* Layout flags.  The arrangement (low two bits) is one of:
+ *   BLOCKROW : rows in order, then columns in order; each block row-major with
+ *              ld = its (rounded) width, stored one after another.
+ *   ROWPANEL : one row-major panel per row sector holding that row's blocks
+ *              side by side in column order; ld = panel width.  A row's blocks
+ *              then form one strided view (the "interleaved" arrangement for
+ *              contraction-axis groups).
+ *   COLPANEL : one panel per column sector with that column's blocks stacked in
+ *              row order; ld = the column's (rounded) width.
+ * CHARGE_SORTED orders sectors by (charge, parity, index) instead of index.
+ * ALIGN16 rounds every block width up to a multiple of 16 bytes, so every
+ * block start and leading dimension is 16-byte aligned (tensor-map rule). */
+enum {
+  BS_LAYOUT_BLOCKROW = 0,
+  BS_LAYOUT_ROWPANEL = 1,
+  BS_LAYOUT_COLPANEL = 2,
+  BS_LAYOUT_CHARGE_SORTED = 4,
+  BS_LAYOUT_ALIGN16 = 8
+};
+
+typedef struct bs_layout bs_layout;
+typedef struct bs_plan bs_plan;
+
+typedef struct bs_block_info {
+  int32_t row;     /* row sector index */
+  int32_t col;     /* column sector index */
+  int64_t offset;  /* first element of the block in the buffer */
+  int32_t rows;    /* = dim of the row sector */
+  int32_t cols;    /* = dim of the column sector */
+  int64_t ld;      /* elements between consecutive rows of the block */
+} bs_block_info;
+
+/* Build the layout of a tensor over (rows x cols) whose populated blocks are
+ * those the rule allows.  elem_bytes (2, 4 or 8) matters only for ALIGN16.
+ * Errors: INVALID_ARG (NULL, n < 0, dim < 1, z2 rule without parities, bad
+ * flags or elem_bytes), OVERFLOW (element count beyond int64), OOM. */
+bs_status bs_layout_create(const bs_axis_desc *rows, const bs_axis_desc *cols, const bs_rule *rule,
+                           uint32_t flags, int32_t elem_bytes, bs_layout **out);
+
+/* Number of populated blocks and buffer length in elements (padding included). */
+bs_status bs_layout_query(const bs_layout *layout, int64_t *nblocks, int64_t *nelems);
+
+/* Copy the block table, in storage order, into out[0 .. nblocks-1]. */
+bs_status bs_layout_blocks(const bs_layout *layout, bs_block_info *out);
+
+void bs_layout_destroy(bs_layout *layout);
+
+typedef enum bs_dtype {
+  BS_F64 = 0,      /* A, B, C double; FP64 pipe */
+  BS_BF16_F32 = 1  /* A, B bfloat16; C float; FP32 accumulation on the tensor cores */
+} bs_dtype;
+
+typedef enum bs_axis_policy {
+  BS_AXIS_AUTO = 0,         /* cost model picks contraction or free axis for the plan */
+  BS_AXIS_CONTRACTION = 1,  /* one group per C block, K = concatenated inner blocks */
+  BS_AXIS_FREE = 2,         /* one group per (k, j): stacked A rows, atomic scatter into C */
+  BS_AXIS_NONE = 3          /* one group per (i, k, j) triple: no coalescing (atomic scatter) */
+} bs_axis_policy;
+
+typedef enum bs_pack_policy {
+  BS_PACK_AUTO = 0,    /* cost model: pack bytes against saved per-segment work */
+  BS_PACK_NEVER = 1,   /* zero-copy views only (BF16 path: MISALIGNED if views break TMA rules) */
+  BS_PACK_ALWAYS = 2   /* gather A and B into panel workspaces before every contraction */
+} bs_pack_policy;
+
+/* Planner options.  Call bs_plan_options_default first, then override. */
+typedef struct bs_plan_options {
+  int32_t axis_policy;        /* bs_axis_policy */
+  int32_t pack_policy;        /* bs_pack_policy */
+  uint32_t c_layout_flags;    /* arrangement flags of C (its elem size follows the dtype) */
+  int32_t merge_rows;         /* 1: stack row sectors whose groups share structure and
+                                 whose A and C rows are stride compatible (LocalSpace keys) */
+  int32_t host_only;          /* 1: build the plan on the host only (inspection; no contract) */
+  int32_t ctas_per_sm;        /* 0: choose from occupancy */
+  /* cost-model constants (microseconds, GB/s, GFLOP/s); <= 0 keeps the built-in value */
+  double t_launch_us;         /* fixed cost of one kernel launch on the stream */
+  double t_task_us;           /* fixed cost of one task in the persistent kernel */
+  double t_segment_us;        /* extra cost of one zero-copy view segment inside a task */
+  double pack_gbs;            /* achieved bandwidth of the gather kernel */
+  double fp64_gflops;         /* sustained FP64 pipe rate of the grouped kernel */
+  double atomic_penalty;      /* relative cost of an atomic scatter store vs a plain store */
+  int32_t wait_timeout_ms;    /* limit of every device-side wait (BF16 path); <= 0: 2000 ms */
+  int32_t debug_flags;        /* testing only: BS_DEBUG_WITHHOLD_COPY makes the BF16 producer
+                                 skip its first copy so the consumer's bounded wait runs out
+                                 and the kernel reports BS_ERR_TIMEOUT; 0 in normal use */
+  int32_t reserved[6];
+} bs_plan_options;
+
+enum { BS_DEBUG_WITHHOLD_COPY = 1 };
+
+void bs_plan_options_default(bs_plan_options *opts);
+
+typedef struct bs_plan_stats {
+  int64_t triples;            /* populated (i, k, j) block GEMMs */
+  int64_t c_blocks;           /* populated C blocks */
+  int64_t groups;             /* coalesced groups (one GEMM each) */
+  int64_t tasks;              /* persistent-kernel work items */
+  int64_t tile_tasks;         /* CTA-wide tiles */
+  int64_t tail_tasks;         /* warp bundles of tiny groups */
+  int64_t segments;           /* zero-copy view segments over all groups */
+  int64_t packed_bytes;       /* bytes gathered per contraction (0: zero-copy) */
+  int64_t workspace_bytes;    /* device workspace owned by the plan */
+  int32_t axis;               /* bs_axis_policy actually used */
+  int32_t packed_a;           /* 1 if A is gathered */
+  int32_t packed_b;           /* 1 if B is gathered */
+  int32_t launches;           /* kernels one bs_contract enqueues */
+  double useful_flops;        /* sum over triples of 2 * d_i * d_k * d_j */
+  double useful_bytes;        /* populated A + B elements read once, C written once */
+  double executed_flops;      /* flops the kernels issue, tile padding included */
+  double model_us;            /* cost-model estimate of one contraction */
+  double model_us_alt;        /* estimate for the other axis / pack choice */
+  double plan_ms;             /* host time spent in bs_plan_create */
+} bs_plan_stats;
+
+/* Build the contraction plan for C = A B.  A's column axis and B's row axis
+ * must be identical (same n, charges, parities, dims) or SHAPE_MISMATCH.
+ * dtype fixes the element types; elem_bytes of the layouts must match it
+ * (8 for F64; 2 for BF16 inputs).  C's layout is built by the plan over
+ * (A rows, B cols) with the structural product as its populated set and
+ * opts->c_layout_flags as arrangement; get it with bs_plan_c_layout.
+ * The plan copies what it needs: A and B layouts may be destroyed afterwards.
+ * Device tables and workspaces are allocated here (cudaMalloc) on the current
+ * device, unless opts->host_only.  Errors: INVALID_ARG, SHAPE_MISMATCH,
+ * UNSUPPORTED, OOM, CUDA, OVERFLOW. */
+bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype,
+                         const bs_plan_options *opts, bs_plan **out);
+
+/* C's layout, owned by the plan (valid until bs_plan_destroy). */
+const bs_layout *bs_plan_c_layout(const bs_plan *plan);
+
+bs_status bs_plan_stats_get(const bs_plan *plan, bs_plan_stats *out);
+
+/* Group table for inspection: for each group g, out[g*8 + 0..7] =
+ * {axis (1 contraction, 2 free, 3 none), M, N, K, m_segments, k_segments,
+ *  first C block row sector, first C block column sector}.
+ * Call with out = NULL to get the count in *ngroups. */
+bs_status bs_plan_groups(const bs_plan *plan, int64_t *ngroups, int64_t *out);
+
+/* Triple coverage for inspection: for each group, the (i, k, j) triples it
+ * computes, as out[3*t .. 3*t+2], group by group; group_ptr[g] .. group_ptr[g+1]
+ * delimit group g.  Pass NULL arrays to get the sizes. */
+bs_status bs_plan_triples(const bs_plan *plan, int64_t *ntriples, int64_t *ngroups, int64_t *group_ptr,
+                          int32_t *out);
+
+/* Enqueue C = A B on `stream` and return at once.  A, B, C are device
+ * pointers to buffers laid out per the plan's A, B and C layouts; every
+ * populated C element is overwritten, padding and absent blocks are not
+ * touched.  A, B and C must not overlap.  Work: an optional gather, an optional
+ * zero fill of C, one persistent grouped-GEMM kernel.  BF16 plans need A and B
+ * 16-byte aligned (MISALIGNED otherwise).  A plan holds one workspace and one
+ * work counter: do not run the same plan on two streams at once.  Errors found
+ * on the device are reported by bs_plan_last_device_error. */
+bs_status bs_contract(bs_plan *plan, const void *A, const void *B, void *C, void *stream);
+
+/* The same contraction on HOST buffers: copies A and B to plan-owned device
+ * buffers (allocated on first use), contracts, copies C back into C_host
+ * (which must hold the C layout's element count; only populated elements are
+ * written) and synchronizes the stream before returning.  Pinned host memory
+ * gives the fastest copies. */
+bs_status bs_contract_host(bs_plan *plan, const void *A_host, const void *B_host, void *C_host,
+                           void *stream);
+
+/* The uncoalesced control: zero the whole C buffer (padding included), then
+ * one kernel launch per populated (i, k, j) triple on `stream`, each adding
+ * A[i,k] B[k,j] into C[i,j] with a plain one-output-per-thread kernel.  It is
+ * the one-launch-per-block baseline that coalescing is measured against
+ * (design note "block coalescing", Summary: tiny GEMMs are launch-bound). */
+bs_status bs_contract_uncoalesced(bs_plan *plan, const void *A, const void *B, void *C, void *stream);
+
+/* Synchronize `stream`, read and clear the plan's device status word.
+ * Returns BS_OK, or the error a kernel recorded (TIMEOUT, DEVICE, ...). */
+bs_status bs_plan_last_device_error(bs_plan *plan, void *stream);
+
+void bs_plan_destroy(bs_plan *plan);
+
+const char *bs_status_string(bs_status status);
+
+/* Library build identification, e.g. "bs 0.1 sm_103a". */
+const char *bs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BS_H */

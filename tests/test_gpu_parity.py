@@ -1,0 +1,214 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on a GB300.
+
+Small workloads are compared on every output block; the full-size workloads
+in the launch configuration the bench times are compared on sampled blocks
+the oracle computes one by one.  FP64: max per-block relative Frobenius error
+1e-12; BF16 inputs with FP32 accumulation: 5e-3 against the FP64 oracle on the
+same BF16 inputs.  Integer-valued inputs make every partial sum exact, so
+there the GPU must match bit for bit in any summation order, atomic scatter
+included.  Block tables and offsets are compared exactly.
+"""
+import numpy as np
+import pytest
+
+import bsgen
+import oracle
+from harness import TOL, check_blocks, operand_host, sort_rc
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU-only machines, skipped there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import block_sparse_tensor_gb300 as bs  # noqa: E402
+
+
+class Run:
+    """Library layouts, plan and device buffers for one workload."""
+
+    def __init__(self, w, la=None, lb=None, lc=None, **opts):
+        self.w = w
+        eb = 2 if w.dtype == "bf16" else 8
+        self.la, self.lb, self.lc = la or w.layout_a, lb or w.layout_b, lc or w.layout_c
+        self.A = bs.Layout(w.rows, w.inner, w.rule_a, self.la, eb)
+        self.B = bs.Layout(w.inner, w.cols, w.rule_b, self.lb, eb)
+        dt = bs.BF16_F32 if w.dtype == "bf16" else bs.F64
+        self.P = bs.Plan(self.A, self.B, dt, c_layout_flags=self.lc, **opts)
+        self.a_host = operand_host(w, 0, self.A.blocks(), self.A.nelems)
+        self.b_host = operand_host(w, 1, self.B.blocks(), self.B.nelems)
+        tdt = torch.int16 if w.dtype == "bf16" else torch.float64
+        self.a = torch.from_numpy(self.a_host.view(np.int16) if w.dtype == "bf16" else self.a_host).to("cuda")
+        self.b = torch.from_numpy(self.b_host.view(np.int16) if w.dtype == "bf16" else self.b_host).to("cuda")
+        self.cdt = torch.float32 if w.dtype == "bf16" else torch.float64
+        self.c = torch.full((max(self.P.c_layout.nelems, 1),), float("nan"), dtype=self.cdt, device="cuda")
+        del tdt
+
+    def run(self, fn=None):
+        (fn or bs.contract)(self.P, self.a, self.b, self.c)
+        torch.cuda.synchronize()
+        assert bs.last_device_error(self.P) == 0
+        return self.c.cpu().numpy().astype(np.float64)
+
+
+def oracle_for(run: Run):
+    return oracle.problem(run.w, run.la, run.lb, run.lc)
+
+
+def compare(run: Run, c_got: np.ndarray, sel=None, exact=False):
+    pr = oracle_for(run)
+    lib_c = sort_rc(run.P.c_layout.blocks())
+    assert np.array_equal(lib_c, pr.lc.blocks()), "C block table differs from the oracle's"
+    C, S = oracle.contract(pr, sel)
+    blocks = lib_c
+    if sel is not None:
+        keep = {(int(i), int(j)) for i, j in np.asarray(sel).reshape(-1, 2)}
+        blocks = np.array([b for b in lib_c if (int(b[0]), int(b[1])) in keep])
+    tol = 0.0 if exact else TOL[run.w.dtype]
+    ok, worst, ncancel = check_blocks(c_got, C, S, blocks, tol)
+    assert ok, f"worst per-block relative error {worst:.3e} > {tol} ({ncancel} cancelling blocks)"
+    return worst
+
+
+def sample_blocks(run: Run, budget_flops: float, seed: int = 0, n_random: int = 400):
+    """Output blocks for the oracle: the costliest one, plus random ones within a flop budget."""
+    ptr, tr = run.P.triples()
+    w = run.w
+    fl = {}
+    for i, k, j in tr:
+        fl[(int(i), int(j))] = fl.get((int(i), int(j)), 0) + 2 * int(w.rows.d[i]) * int(w.inner.d[k]) * int(w.cols.d[j])
+    keys = list(fl)
+    rng = np.random.default_rng(seed)
+    pick = [max(keys, key=lambda x: fl[x])]
+    used = fl[pick[0]]
+    for t in rng.permutation(len(keys))[: n_random * 4]:
+        kk = keys[t]
+        if kk in pick or used + fl[kk] > budget_flops:
+            continue
+        pick.append(kk)
+        used += fl[kk]
+        if len(pick) > n_random:
+            break
+    return np.array(pick, np.int32)
+
+
+# ---------------------------------------------------------------- small workloads, every block
+POLICIES = {
+    "auto": {},
+    "contraction": dict(axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_NEVER),
+    "free": dict(axis_policy=bs.AXIS_FREE, pack_policy=bs.PACK_NEVER),
+    "none": dict(axis_policy=bs.AXIS_NONE),
+    "contraction_pack": dict(axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS),
+    "free_pack": dict(axis_policy=bs.AXIS_FREE, pack_policy=bs.PACK_ALWAYS),
+}
+LAYOUTS = {"panels": (None, None, None), "blockrow": ("blockrow", "blockrow", "blockrow"),
+           "mixed": ("colpanel", "rowpanel|charge_sorted", "rowpanel")}
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+@pytest.mark.parametrize("pol", sorted(POLICIES))
+@pytest.mark.parametrize("lay", sorted(LAYOUTS))
+def test_fp64_small_configs_every_block(cfg, pol, lay):
+    r = Run(bsgen.get(cfg), *LAYOUTS[lay], **POLICIES[pol])
+    compare(r, r.run())
+
+
+@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("pol", ["contraction", "free", "none", "contraction_pack", "auto"])
+def test_integer_inputs_bit_exact(seed, pol):
+    w = bsgen.tiny_random(seed, values="int3", max_sectors=14, max_dim=40 if seed % 4 == 0 else 9)
+    r = Run(w, *LAYOUTS[["panels", "blockrow", "mixed"][seed % 3]], **POLICIES[pol])
+    compare(r, r.run(), exact=True)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_bf16_integer_inputs_bit_exact(seed):
+    """|x| <= 3 integers are exact in bfloat16 and every FP32 partial sum stays exact."""
+    w = bsgen.tiny_random(50 + seed, values="int3", dtype="bf16", max_sectors=10, max_dim=70 if seed % 2 else 20)
+    r = Run(w, "rowpanel|align16", "colpanel|align16", "rowpanel|align16")
+    compare(r, r.run(), exact=True)
+    r2 = Run(w, "blockrow", "blockrow", "blockrow")      # gathered into aligned panels first
+    assert r2.P.stats()["packed_a"] == 1
+    compare(r2, r2.run(), exact=True)
+
+
+@pytest.mark.parametrize("mkn", [(1, 1, 1), (7, 5, 3), (128, 64, 16), (129, 257, 65), (300, 700, 40), (1024, 96, 1024)])
+@pytest.mark.parametrize("dtype", ["f64", "bf16"])
+def test_single_sector_is_a_dense_gemm(mkn, dtype):
+    m, k, n = mkn
+    w = bsgen.Workload("dense", dtype, bsgen.Axis([0], [m]), bsgen.Axis([0], [k]), bsgen.Axis([0], [n]),
+                       bsgen.Rule(0, 0), bsgen.Rule(0, 0), "uniform", 1234 + m + k + n)
+    lay = ("blockrow|align16",) * 3 if dtype == "bf16" else ("blockrow",) * 3
+    r = Run(w, *lay)
+    compare(r, r.run())
+
+
+def test_poisoned_c_only_populated_elements_written():
+    """C starts as NaN: every populated element is written, padding keeps its NaN."""
+    w = bsgen.config4()
+    w.rows, w.inner, w.cols = (bsgen.Axis(a.q[:40], a.d[:40]) if a.n == 100 else bsgen.Axis(a.q[:10], a.d[:10])
+                               for a in (w.rows, w.inner, w.cols))
+    r = Run(w)
+    c = r.run()
+    idx = np.zeros(r.P.c_layout.nelems, bool)
+    from harness import element_index
+    idx[element_index(r.P.c_layout.blocks())] = True
+    assert not np.any(np.isnan(c[idx]))
+    assert np.all(np.isnan(c[~idx])) and (~idx).sum() > 0
+    compare(r, c)
+
+
+def test_repeated_calls_are_identical():
+    r = Run(bsgen.config2(), axis_policy=bs.AXIS_CONTRACTION)
+    c1 = r.run()
+    c2 = r.run()
+    assert np.array_equal(c1, c2)          # one writer per C element: deterministic
+
+
+def test_host_buffer_entry_point_matches_device_entry_point():
+    r = Run(bsgen.config2())
+    c_dev = r.run()
+    c_host = np.zeros(r.P.c_layout.nelems, np.float64)
+    bs.contract_host(r.P, r.a_host, r.b_host, c_host)
+    assert np.array_equal(c_host, c_dev)
+
+
+def test_uncoalesced_control_matches_oracle():
+    r = Run(bsgen.config2())
+    c = r.run(bs.contract_uncoalesced)
+    compare(r, c)
+
+
+def test_bf16_wait_timeout_is_reported_and_context_survives():
+    """A producer that withholds one copy makes the consumer's bounded wait run out;
+    the kernel reports BS_ERR_TIMEOUT and the context stays usable."""
+    w = bsgen.config4()
+    r = Run(w, wait_timeout_ms=50, debug_flags=1)
+    bs.contract(r.P, r.a, r.b, r.c)
+    assert bs.last_device_error(r.P) == 6
+    r2 = Run(w)
+    compare(r2, r2.run(), sel=sample_blocks(r2, 2e8, n_random=60))
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled blocks
+@pytest.mark.parametrize("cfg", [3, 4, 5])
+def test_full_size_sampled_blocks(cfg):
+    w = bsgen.get(cfg)
+    r = Run(w)
+    c = r.run()
+    from harness import element_index
+    assert not np.any(np.isnan(c[element_index(r.P.c_layout.blocks())]))   # every populated element written
+    compare(r, c, sel=sample_blocks(r, 1.5e9 if cfg != 5 else 2.5e9, seed=cfg))
+
+
+def test_config5_pack_path_sampled_blocks():
+    w = bsgen.config5()
+    r = Run(w, "blockrow", "blockrow", "blockrow", axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)
+    compare(r, r.run(), sel=sample_blocks(r, 1.0e9, seed=11))
+
+
+def test_config4_blockrow_gather_path_sampled_blocks():
+    w = bsgen.config4()
+    r = Run(w, w.pack_layout_a, w.pack_layout_b, w.pack_layout_c)
+    assert r.P.stats()["packed_a"] == 1
+    compare(r, r.run(), sel=sample_blocks(r, 1.0e9, seed=4))

@@ -1,0 +1,220 @@
+"""Host-side checks of libbs.so that need no GPU.
+
+- the shared library loads and exports every entry point include/bs.h declares;
+- layouts built by the library equal the oracle's layouts bit for bit;
+- host-only plans cover every populated triple exactly once, with hole-free
+  single-axis groups, and build the same C layout as the oracle;
+- argument errors come back as status codes.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import bsgen
+import oracle
+
+bs = pytest.importorskip("block_sparse_tensor_gb300")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_library_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "bs.h")).read()
+    declared = set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(bs_\w+)\s*\(", header, re.M))
+    assert len(declared) >= 15
+    for name in declared:
+        assert hasattr(bs.lib, name), f"{name} declared but not exported"
+    assert set(bs.EXPORTED) <= declared
+    assert bs.version().startswith("bs ")
+
+
+LAYOUT_FLAGS = ["blockrow", "rowpanel", "colpanel", "blockrow|charge_sorted", "rowpanel|charge_sorted",
+                "colpanel|charge_sorted", "rowpanel|align16", "colpanel|charge_sorted|align16", "blockrow|align16"]
+
+
+def lib_blocks_by_rc(layout):
+    b = layout.blocks()
+    order = np.lexsort((b[:, 1], b[:, 0]))
+    return b[order]
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+@pytest.mark.parametrize("flags", LAYOUT_FLAGS)
+def test_layout_matches_oracle(cfg, flags):
+    w = bsgen.get(cfg)
+    eb = 2 if w.dtype == "bf16" else 8
+    for ax_r, ax_c, rule in [(w.rows, w.inner, w.rule_a), (w.inner, w.cols, w.rule_b)]:
+        L = bs.Layout(ax_r, ax_c, rule, flags, eb)
+        mask = oracle.rule_mask(ax_r, ax_c, rule)
+        ol = oracle.layout(ax_r, ax_c, mask, flags, eb)
+        assert L.nelems == ol.nelems
+        assert np.array_equal(lib_blocks_by_rc(L), ol.blocks())
+
+
+def test_layout_matches_oracle_config5():
+    w = bsgen.config5()
+    for flags in ["blockrow", "rowpanel|charge_sorted", "colpanel|charge_sorted"]:
+        L = bs.Layout(w.rows, w.inner, w.rule_a, flags, 8)
+        ol = oracle.layout(w.rows, w.inner, oracle.rule_mask(w.rows, w.inner, w.rule_a), flags, 8)
+        assert L.nelems == ol.nelems
+        assert np.array_equal(lib_blocks_by_rc(L), ol.blocks())
+
+
+def host_plan(w, la=None, lb=None, **opts):
+    eb = 2 if w.dtype == "bf16" else 8
+    A = bs.Layout(w.rows, w.inner, w.rule_a, la or w.layout_a, eb)
+    B = bs.Layout(w.inner, w.cols, w.rule_b, lb or w.layout_b, eb)
+    dt = bs.BF16_F32 if w.dtype == "bf16" else bs.F64
+    opts.setdefault("c_layout_flags", w.layout_c)
+    return bs.Plan(A, B, dt, host_only=1, **opts), A, B
+
+
+def oracle_triples(w):
+    ma = oracle.rule_mask(w.rows, w.inner, w.rule_a).astype(bool)
+    mb = oracle.rule_mask(w.inner, w.cols, w.rule_b).astype(bool)
+    out = set()
+    for i, k in zip(*np.nonzero(ma)):
+        for j in np.nonzero(mb[k])[0]:
+            out.add((int(i), int(k), int(j)))
+    return out, ma, mb
+
+
+POLICIES = [dict(axis_policy=bs.AXIS_CONTRACTION), dict(axis_policy=bs.AXIS_FREE), dict(axis_policy=bs.AXIS_NONE),
+            dict(axis_policy=bs.AXIS_AUTO), dict(axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS),
+            dict(axis_policy=bs.AXIS_FREE, pack_policy=bs.PACK_ALWAYS)]
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3])
+@pytest.mark.parametrize("pol", range(len(POLICIES)))
+@pytest.mark.parametrize("lay", [(None, None), ("blockrow", "blockrow")])
+def test_plan_covers_each_triple_once_and_is_hole_free(cfg, pol, lay):
+    w = bsgen.get(cfg)
+    P, A, B = host_plan(w, *lay, **POLICIES[pol])
+    want, ma, mb = oracle_triples(w)
+    ptr, tr = P.triples()
+    got = [tuple(int(x) for x in t) for t in tr]
+    assert len(got) == len(set(got)) == len(want)
+    assert set(got) == want
+    st = P.stats()
+    assert st["triples"] == len(want)
+    # every group is one axis: a contraction group has one (i, j) (or stacked i's
+    # with the same k list); a free group has one (k, j); nothing else
+    for g in range(len(ptr) - 1):
+        t = tr[ptr[g]:ptr[g + 1]]
+        ks = {int(x) for x in t[:, 1]}
+        js = {int(x) for x in t[:, 2]}
+        is_ = {int(x) for x in t[:, 0]}
+        assert len(js) == 1
+        if st["axis"] == bs.AXIS_CONTRACTION:
+            # hole-free: every (i, k) pair of the rectangle exists
+            for i in is_:
+                for k in ks:
+                    assert ma[i, k] and mb[k, next(iter(js))]
+        elif st["axis"] == bs.AXIS_FREE:
+            assert len(ks) == 1
+        else:
+            assert len(t) == 1
+    flops = sum(2 * int(w.rows.d[i]) * int(w.inner.d[k]) * int(w.cols.d[j]) for (i, k, j) in want)
+    assert st["useful_flops"] == pytest.approx(flops, rel=1e-12)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 4])
+def test_plan_c_layout_matches_oracle(cfg):
+    w = bsgen.get(cfg)
+    P, _, _ = host_plan(w)
+    pr = oracle.problem(w)
+    assert P.c_layout.nelems == pr.lc.nelems
+    assert np.array_equal(lib_blocks_by_rc(P.c_layout), pr.lc.blocks())
+
+
+def test_localspace_keys_merge_into_taller_groups():
+    """Config 4: the four LocalSpace key rows of a charge share every inner block and
+    sit in consecutive row panels with one stride, so they stack into one group."""
+    w = bsgen.config4()
+    P, _, _ = host_plan(w)
+    g = P.groups()
+    st = P.stats()
+    assert st["triples"] == 1404
+    assert st["c_blocks"] == 652
+    assert len(g) == 652 // 4
+    assert np.all(g[:, 1] % 4 == 0)
+    P2, _, _ = host_plan(w, merge_rows=0)
+    assert len(P2.groups()) == 652
+
+
+def test_band_layouts_give_single_view_groups():
+    """Row-panel A and column-panel B sorted by charge turn every contraction-axis
+    group of the band and parity rules into one strided view (zero copy)."""
+    for cfg in (1, 2, 3):
+        P, _, _ = host_plan(bsgen.get(cfg), axis_policy=bs.AXIS_CONTRACTION)
+        g = P.groups()
+        assert np.all(g[:, 5] == 1)
+    w5 = bsgen.config5()
+    P5, _, _ = host_plan(w5, axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_NEVER)
+    assert np.all(P5.groups()[:, 5] == 1)
+    assert P5.stats()["triples"] > 4_000_000
+
+
+def test_blockrow_layout_fragments_groups_and_pack_merges_them():
+    w = bsgen.config2()
+    P, _, _ = host_plan(w, "blockrow", "blockrow", axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_NEVER)
+    assert np.any(P.groups()[:, 5] > 1)
+    Pk, _, _ = host_plan(w, "blockrow", "blockrow", axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)
+    assert np.all(Pk.groups()[:, 5] == 1)
+    st = Pk.stats()
+    assert st["packed_a"] == 1 and st["packed_b"] == 1 and st["packed_bytes"] > 0
+
+
+def test_bf16_misaligned_views_are_packed_or_refused():
+    w = bsgen.config4()
+    P, _, _ = host_plan(w, "blockrow", "blockrow")
+    assert P.stats()["packed_a"] == 1
+    with pytest.raises(bs.BsError) as e:
+        host_plan(w, "blockrow", "blockrow", pack_policy=bs.PACK_NEVER)
+    assert e.value.code == 7
+    P2, _, _ = host_plan(w)
+    assert P2.stats()["packed_a"] == 0
+
+
+def test_errors_are_status_codes():
+    w = bsgen.config1()
+    A = bs.Layout(w.rows, w.inner, w.rule_a, "blockrow", 8)
+    other = bsgen.Axis(np.arange(-4, 5), np.ones(9))
+    Bbad = bs.Layout(other, w.cols, w.rule_b, "blockrow", 8)
+    with pytest.raises(bs.BsError) as e:
+        bs.Plan(A, Bbad, bs.F64, host_only=1)
+    assert e.value.code == 2
+    with pytest.raises(bs.BsError) as e:
+        bs.Plan(A, A, bs.BF16_F32, host_only=1)
+    assert e.value.code == 1
+    with pytest.raises(bs.BsError) as e:
+        bs.Layout(w.rows, w.inner, bsgen.Rule(0, 0, True), "blockrow", 8)   # parity rule without parities
+    assert e.value.code == 1
+    with pytest.raises(bs.BsError) as e:
+        bs.Layout(w.rows, w.inner, w.rule_a, 3, 8)
+    assert e.value.code == 1
+    with pytest.raises(bs.BsError) as e:
+        bs.Layout(bsgen.Axis([0], [0]), w.inner, w.rule_a, 0, 8)
+    assert e.value.code == 1
+    w4 = bsgen.config4()
+    A4 = bs.Layout(w4.rows, w4.inner, w4.rule_a, w4.layout_a, 2)
+    B4 = bs.Layout(w4.inner, w4.cols, w4.rule_b, w4.layout_b, 2)
+    with pytest.raises(bs.BsError) as e:
+        bs.Plan(A4, B4, bs.BF16_F32, host_only=1, axis_policy=bs.AXIS_FREE)
+    assert e.value.code == 3
+    assert bs.lib.bs_status_string(2) == b"shape mismatch"
+    P = bs.Plan(A, bs.Layout(w.inner, w.cols, w.rule_b, "blockrow", 8), bs.F64, host_only=1)
+    with pytest.raises(bs.BsError):
+        bs.contract(P, 0, 0, 0)
+
+
+def test_empty_structure():
+    """A rule that admits no block gives an empty plan and an empty C."""
+    w = bsgen.config1()
+    A = bs.Layout(w.rows, w.inner, bsgen.Rule(50, 60), "blockrow", 8)
+    B = bs.Layout(w.inner, w.cols, w.rule_b, "blockrow", 8)
+    P = bs.Plan(A, B, bs.F64, host_only=1)
+    st = P.stats()
+    assert st["triples"] == 0 and st["c_blocks"] == 0 and P.c_layout.nelems == 0
