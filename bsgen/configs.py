@@ -155,8 +155,8 @@ def config4() -> Workload:
                     Rule(-2, 2), Rule(-1, 1), "uniform", 0x5EED0000 + 4,
                     layout_a="rowpanel|charge_sorted|align16", layout_b="colpanel|charge_sorted|align16",
                     layout_c="rowpanel|charge_sorted|align16",
-                    pack_layout_a="blockrow|align16", pack_layout_b="blockrow|align16",
-                    pack_layout_c="blockrow|align16", extra={"key_dim": 4})
+                    pack_layout_a="blockrow", pack_layout_b="blockrow",
+                    pack_layout_c="blockrow", extra={"key_dim": 4})
 
 
 def random_sector_axis(s: rng.SplitMix64, n: int, n_big: int, big_dim: int, qlo: int, qhi: int,

@@ -127,7 +127,7 @@ def test_bf16_integer_inputs_bit_exact(seed):
     w = bsgen.tiny_random(50 + seed, values="int3", dtype="bf16", max_sectors=10, max_dim=70 if seed % 2 else 20)
     r = Run(w, "rowpanel|align16", "colpanel|align16", "rowpanel|align16")
     compare(r, r.run(), exact=True)
-    r2 = Run(w, "blockrow", "blockrow", "blockrow")      # gathered into aligned panels first
+    r2 = Run(w, "blockrow", "blockrow", "blockrow", pack_policy=bs.PACK_ALWAYS)   # gathered into aligned panels
     assert r2.P.stats()["packed_a"] == 1
     compare(r2, r2.run(), exact=True)
 
