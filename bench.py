@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark of the coalesced block-sparse contraction C[i,j] = sum_k A[i,k] B[k,j].
+
+One step = one bs_contract over the headline workload (default: the FP64
+"tail" workload of 31 U(1) sectors per axis, d(q) = max(1, round(64 e^{-q^2/50}))),
+inputs resident in HBM, L2 flushed between steps by a 256 MiB write.  Prints
+one JSON line: useful GFLOP/s (sum over populated triples of 2 d_i d_k d_j per
+second), blocks/s (populated triples per second), the roofline of the grouped
+kernel, an end-to-end number through the host-buffer entry point, the CPU
+oracle on the host cores, sampled clocks, and a per-workload summary of all
+five synthetic workloads with the one-launch-per-triple control beside them.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--config n]
+
+For N > 1 (torchrun) every rank runs its own replica of the workload (weak
+scaling); the only collectives are the timing barrier and the max over ranks.
+`--impl reference` times the CPU oracle instead, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import bsgen  # noqa: E402
+
+METRIC = "useful GFLOP/s + blocks/s per contraction; fraction of FP64/BF16 roofline"
+FP64_FLOP_PER_CLK_PER_SM = 4          # 1.25 TFLOP/s nominal over 152 SMs at 2070 MHz
+NOMINAL_SMS, NOMINAL_MAX_MHZ = 152, 2070.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return {}
+
+
+def workload_desc(w: bsgen.Workload) -> str:
+    return (f"{w.name}: {w.rows.n}x{w.inner.n}x{w.cols.n} sectors, rules A {w.rule_a.dq_min}..{w.rule_a.dq_max}"
+            f"{' +parity' if w.rule_a.z2 else ''}, B {w.rule_b.dq_min}..{w.rule_b.dq_max}, values {w.values}, "
+            f"layouts A={w.layout_a} B={w.layout_b} C={w.layout_c}")
+
+
+# ------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while it runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.dev = device_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                mhz.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                pass
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------------- GPU arm
+class Problem:
+    """Layouts, plan and resident device buffers of one workload."""
+
+    def __init__(self, bs, torch, w: bsgen.Workload, **opts):
+        self.w = w
+        eb = 2 if w.dtype == "bf16" else 8
+        self.A = bs.Layout(w.rows, w.inner, w.rule_a, w.layout_a, eb)
+        self.B = bs.Layout(w.inner, w.cols, w.rule_b, w.layout_b, eb)
+        self.P = bs.Plan(self.A, self.B, bs.BF16_F32 if w.dtype == "bf16" else bs.F64, c_layout_flags=w.layout_c, **opts)
+        self.stats = self.P.stats()
+        self.a_host = self._operand(0, self.A)
+        self.b_host = self._operand(1, self.B)
+        self.a = torch.from_numpy(self.a_host).cuda()
+        self.b = torch.from_numpy(self.b_host).cuda()
+        cdt = torch.float32 if w.dtype == "bf16" else torch.float64
+        self.c = torch.zeros(max(self.P.c_layout.nelems, 1), dtype=cdt, device="cuda")
+
+    def _operand(self, op, L):
+        b = L.blocks()
+        vals = self.w.draw(op, b[:, 0], b[:, 1], b[:, 3], b[:, 4])
+        buf = np.zeros(L.nelems)
+        buf[L.element_index(b)] = vals
+        if self.w.dtype == "bf16":
+            return bsgen.rng.bf16_bits(buf).view(np.int16)
+        return buf
+
+
+def time_steps(torch, fn, steps, warmup, flush, stream):
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before every step."""
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in ev]
+
+
+def kernel_source_tag(dtype: str) -> str:
+    src = "bs_bf16.cu" if dtype == "bf16" else "bs_fp64.cu"
+    with open(os.path.join(ROOT, "block_sparse_tensor_gb300", "csrc", src), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def recorded_traffic(workload: str, tag: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        for line in open(path):
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == tag:
+                return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+def roofline(w, stats, kernel_ms, calib, peaks, clock_mhz):
+    if w.dtype == "bf16":
+        # BF16 workload: intensity below the tensor ridge, so HBM bounds it
+        hbm = peaks.get("hbm_gbs") or 6800.0
+        achieved = stats["useful_bytes"] / (kernel_ms * 1e-3) / 1e9
+        out = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+               "peak_source": "MEASURED_PEAKS.json hbm_gbs" if peaks.get("hbm_gbs") else "fallback 6.8 TB/s"}
+    else:
+        peak = NOMINAL_SMS * FP64_FLOP_PER_CLK_PER_SM * NOMINAL_MAX_MHZ * 1e6 / 1e12
+        achieved = stats["useful_flops"] / (kernel_ms * 1e-3) / 1e12
+        out = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+               "peak_source": "FP64 pipe: 152 SMs x 4 flop/clk x 2070 MHz (nominal 1.25 TFLOP/s)",
+               "fp64_probe_tflops": calib["fp64_gflops"] / 1e3 if calib else None}
+        if clock_mhz:
+            out["frac_at_sampled_clock"] = achieved / (peak * clock_mhz / NOMINAL_MAX_MHZ)
+    return out
+
+
+def run_gpu(args):
+    import torch
+
+    import block_sparse_tensor_gb300 as bs
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    peaks = measured_peaks()
+    calib = None if args.skip_calib else bs.calibrate(stream)
+    log(f"[bench] calibration: {calib}")
+
+    w = bsgen.get(args.config)
+    pb = Problem(bs, torch, w)
+    st = pb.stats
+    fn = lambda: bs.contract(pb.P, pb.a, pb.b, pb.c, stream)  # noqa: E731
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    times = time_steps(torch, fn, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    assert bs.last_device_error(pb.P, stream) == 0
+    ms = statistics.mean(times)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * st["useful_flops"] / (ms * 1e-3) / 1e9
+    blocks_s = world * st["triples"] / (ms * 1e-3)
+
+    # end to end through the host-buffer entry point, pinned buffers
+    a_pin = torch.from_numpy(pb.a_host).pin_memory()
+    b_pin = torch.from_numpy(pb.b_host).pin_memory()
+    c_pin = torch.zeros(pb.c.numel(), dtype=pb.c.dtype).pin_memory()
+    bs.contract_host(pb.P, a_pin, b_pin, c_pin, stream)
+    e2e_t = []
+    for _ in range(max(args.steps, 5)):
+        t0 = time.perf_counter()
+        bs.contract_host(pb.P, a_pin, b_pin, c_pin, stream)
+        e2e_t.append(time.perf_counter() - t0)
+    e2e_s = statistics.mean(e2e_t)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f64", "data": "synthetic",
+        "blocks_per_s": blocks_s,
+        "config": {"workload": workload_desc(w), "triples": st["triples"], "c_blocks": st["c_blocks"],
+                   "useful_gflop": st["useful_flops"] / 1e9, "useful_mb": st["useful_bytes"] / 1e6,
+                   "groups": st["groups"], "axis": ["auto", "contraction", "free", "none"][st["axis"]],
+                   "packed": bool(st["packed_a"] or st["packed_b"]),
+                   "l2": "flushed before every step (256 MiB write, untimed)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "gpu_launches": args.steps * st["launches"],
+    }
+    kernel_ms = ms if st["launches"] == 1 else None
+    if kernel_ms is None:
+        kernel_ms = ms  # pack / zero fill share the step; reported as an upper bound on the kernel's time
+    rl = roofline(w, st, kernel_ms, calib, peaks, clocks.get("sm_mhz"))
+    tag = kernel_source_tag(w.dtype)
+    tr = recorded_traffic(w.name, tag)
+    rl["traffic"] = tr
+    rl["kernel"] = "bf16_grouped_kernel" if w.dtype == "bf16" else "fp64_grouped_kernel"
+    rl["kernel_source"] = tag
+    line["roofline"] = rl
+    line["e2e"] = {"value": st["useful_flops"] / e2e_s / 1e9 * world, "unit": "GFLOP/s",
+                   "h2d_bytes_per_step": int(pb.a_host.nbytes + pb.b_host.nbytes),
+                   "d2h_bytes_per_step": int(c_pin.numel() * c_pin.element_size())}
+    line["clocks"] = clocks
+    line["calibration"] = calib
+    line["model_us"] = st["model_us"]
+
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    if not args.skip_configs:
+        del pb
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config(bs, torch, flush, stream, calib, peaks, args, clocks.get("sm_mhz"))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def per_config(bs, torch, flush, stream, calib, peaks, args, clock_mhz):
+    out = {}
+    for n in sorted(bsgen.CONFIGS):
+        w = bsgen.get(n)
+        t0 = time.time()
+        pb = Problem(bs, torch, w)
+        st = pb.stats
+        setup_s = time.time() - t0
+        steps = 10 if n != 1 else 50
+        ms = statistics.median(time_steps(torch, lambda: bs.contract(pb.P, pb.a, pb.b, pb.c, stream), steps, 3,
+                                          flush, stream))
+        assert bs.last_device_error(pb.P, stream) == 0
+        rl = roofline(w, st, ms, calib, peaks, clock_mhz)
+        rec = {"workload": w.name, "dtype": w.dtype, "ms": ms, "gflops": st["useful_flops"] / (ms * 1e-3) / 1e9,
+               "blocks_per_s": st["triples"] / (ms * 1e-3), "triples": st["triples"], "c_blocks": st["c_blocks"],
+               "groups": st["groups"], "tasks": st["tasks"], "useful_gflop": st["useful_flops"] / 1e9,
+               "useful_mb": st["useful_bytes"] / 1e6, "roofline_frac": rl["frac"], "roofline_bound": rl["bound"],
+               "executed_over_useful": st["executed_flops"] / max(st["useful_flops"], 1),
+               "plan_ms": st["plan_ms"], "model_us": st["model_us"], "setup_s": setup_s}
+        if n in (1, 2) or (n == 5 and args.all_configs) or (n in (3, 4) and args.all_configs):
+            ctrl = lambda: bs.contract_uncoalesced(pb.P, pb.a, pb.b, pb.c, stream)  # noqa: E731
+            reps = 3 if n != 5 else 1
+            cms = statistics.median(time_steps(torch, ctrl, reps, 1, flush, stream))
+            rec["control_ms"] = cms
+            rec["speedup_vs_control"] = cms / ms
+            rec["control_launches_per_s"] = st["triples"] / (cms * 1e-3)
+        out[str(n)] = rec
+        log(f"[bench] config {n}: {json.dumps(rec)}")
+        del pb
+        torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------------- CPU oracle
+def cpu_baseline(w: bsgen.Workload, budget_s: float = 12.0):
+    """The oracle as it stands, single-threaded on a host core, on the same workload."""
+    import oracle
+    pr = oracle.problem(w)
+    ma, mb = pr.ma.astype(np.int64), pr.mb.astype(np.int64)
+    flops = 0.0
+    for i, k in zip(*np.nonzero(ma)):
+        js = np.nonzero(mb[k])[0]
+        flops += 2.0 * int(w.rows.d[i]) * int(w.inner.d[k]) * float(w.cols.d[js].astype(np.int64).sum())
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.contract(pr)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (reps >= 1 and el * (reps + 1) / reps > 3 * budget_s):
+            break
+    return {"value": flops * reps / el / 1e9, "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"the full {w.name} contraction, {reps} times in {el:.1f} s (plain C triple loop, FP64)"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    w = bsgen.get(args.config)
+    import oracle
+    pr = oracle.problem(w)
+    ma, mb = pr.ma.astype(np.int64), pr.mb.astype(np.int64)
+    flops, triples = 0.0, 0
+    for i, k in zip(*np.nonzero(ma)):
+        js = np.nonzero(mb[k])[0]
+        triples += len(js)
+        flops += 2.0 * int(w.rows.d[i]) * int(w.inner.d[k]) * float(w.cols.d[js].astype(np.int64).sum())
+    for _ in range(args.warmup):
+        oracle.contract(pr)
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.contract(pr)
+        ts.append(time.perf_counter() - t0)
+    s = statistics.mean(ts)
+    value = flops / s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64" if w.dtype == "f64" else "bf16",
+            "data": "synthetic", "blocks_per_s": triples / s,
+            "config": {"workload": workload_desc(w), "triples": triples, "parallelism": "host core"},
+            "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step is the full {w.name} contraction by the plain C oracle"},
+            "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", type=int, default=2, choices=sorted(bsgen.CONFIGS))
+    ap.add_argument("--all-configs", action="store_true", help="also time the control on configs 3-5")
+    ap.add_argument("--skip-configs", action="store_true", help="headline workload only")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--skip-calib", action="store_true", help="skip the probe kernels (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -31,7 +31,7 @@ EXPORTED = ["bs_layout_create", "bs_layout_query", "bs_layout_blocks", "bs_layou
             "bs_plan_options_default", "bs_plan_create", "bs_plan_c_layout", "bs_plan_stats_get",
             "bs_plan_groups", "bs_plan_triples", "bs_contract", "bs_contract_host",
             "bs_contract_uncoalesced", "bs_plan_last_device_error", "bs_plan_destroy",
-            "bs_status_string", "bs_version"]
+            "bs_status_string", "bs_version", "bs_calibrate"]
 
 
 class BsError(RuntimeError):
@@ -75,6 +75,12 @@ class PlanStats(ctypes.Structure):
                 ("model_us", ctypes.c_double), ("model_us_alt", ctypes.c_double), ("plan_ms", ctypes.c_double)]
 
 
+class Calibration(ctypes.Structure):
+    _fields_ = [("fp64_gflops", ctypes.c_double), ("fp64_gflops_quarter_warp", ctypes.c_double),
+                ("launch_us", ctypes.c_double), ("copy_gbs", ctypes.c_double), ("sm_count", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 7)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libbs.so is not built ({LIB_PATH}); run block_sparse_tensor_gb300.build.build()")
@@ -99,6 +105,7 @@ def _load():
         "bs_plan_destroy": (None, [P]),
         "bs_status_string": (ctypes.c_char_p, [st]),
         "bs_version": (ctypes.c_char_p, []),
+        "bs_calibrate": (st, [P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -198,6 +205,20 @@ class Layout:
             out[t] = (b.row, b.col, b.offset, b.rows, b.cols, b.ld)
         return out
 
+    def element_index(self, blocks: Optional[np.ndarray] = None) -> np.ndarray:
+        """Buffer index of every element of every block, block after block in the
+        given (default: storage) order, row-major inside a block.  Filling
+        buf[layout.element_index()] = values places block-concatenated values."""
+        b = self.blocks() if blocks is None else blocks
+        if len(b) == 0:
+            return np.zeros(0, np.int64)
+        sizes = b[:, 3] * b[:, 4]
+        starts = np.concatenate([[0], np.cumsum(sizes)[:-1]])
+        rep = np.repeat(np.arange(len(b)), sizes)
+        local = np.arange(int(sizes.sum()), dtype=np.int64) - starts[rep]
+        c = b[rep, 4]
+        return b[rep, 2] + (local // c) * b[rep, 5] + local % c
+
     def __del__(self):
         if getattr(self, "_own", False) and self.h:
             lib.bs_layout_destroy(self.h)
@@ -272,6 +293,13 @@ def contract_uncoalesced(plan: Plan, A, B, C, stream=None):
 def last_device_error(plan: Plan, stream=None) -> int:
     """Synchronize and return (and clear) the device status as a bs_status code."""
     return int(lib.bs_plan_last_device_error(plan.h, _stream(stream)))
+
+
+def calibrate(stream=None) -> dict:
+    """Measure the cost-model constants on the current device (bs_calibrate)."""
+    c = Calibration()
+    _check(lib.bs_calibrate(ctypes.byref(c), _stream(stream)), "bs_calibrate")
+    return {name: getattr(c, name) for name, _ in Calibration._fields_ if name != "reserved"}
 
 
 def version() -> str:

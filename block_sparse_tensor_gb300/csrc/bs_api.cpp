@@ -132,19 +132,21 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-bs_status encode_maps(bs_plan *P, const void *A, const void *B) {
+bs_status encode_maps(bs_plan *P, const void *A, const void *B, const void *C) {
   auto enc = get_encode();
   if (!enc) return BS_ERR_CUDA;
   P->map_bytes.assign(P->maps.size() * sizeof(CUtensorMap), 0);
   for (size_t t = 0; t < P->maps.size(); ++t) {
     const MapDesc &m = P->maps[t];
-    const char *base = (const char *)(m.operand == 0 ? A : B) + m.off * 2;
+    const int eb = m.operand == 2 ? 4 : 2;
+    const char *base = (const char *)(m.operand == 0 ? A : m.operand == 1 ? B : C) + m.off * eb;
     cuuint64_t dims[2] = {(cuuint64_t)m.inner, (cuuint64_t)m.outer};
-    cuuint64_t strides[1] = {(cuuint64_t)(m.ld * 2)};
+    cuuint64_t strides[1] = {(cuuint64_t)(m.ld * eb)};
     cuuint32_t box[2] = {(cuuint32_t)m.box_inner, (cuuint32_t)m.box_outer};
     cuuint32_t es[2] = {1, 1};
     CUtensorMap *out = (CUtensorMap *)(P->map_bytes.data() + t * sizeof(CUtensorMap));
-    CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)base, dims, strides, box, es,
+    CUresult r = enc(out, m.operand == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     (void *)base, dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return BS_ERR_MISALIGNED;
@@ -191,6 +193,8 @@ void build_bf16(bs_plan *P) {
         t.bn = (std::min(256, g.n - n0) + 15) / 16 * 16;
         t.c_off = rs.rc;
         t.ldc = rs.ldc;
+        // C is written by TMA stores when its view obeys the 16-byte rules
+        t.map_c = tma_ok(rs.rc, rs.ldc, 4) ? map_id(2, rs.rc, g.n, g.m, rs.ldc, 32, 32) : -1;
         int64_t kch = 0;
         for (int32_t s = 0; s < g.kseg_count; ++s) kch += (gs.ksegs[g.kseg_begin + s].klen + 63) / 64;
         costed.push_back({(double)kch * (t.bn + 64), t});
@@ -207,7 +211,7 @@ bs_status upload(bs_plan *P) {
   size_t o_groups = append_bytes(buf, P->gs.groups);
   size_t o_rsegs = append_bytes(buf, P->gs.rsegs);
   size_t o_ksegs = append_bytes(buf, P->gs.ksegs);
-  size_t o_tail = append_bytes(buf, P->ts.tail_groups);
+  size_t o_tail = append_bytes(buf, P->ts.tail_elems);
   size_t o_pack = append_bytes(buf, P->pack_copies);
   size_t o_zero = append_bytes(buf, P->zero_blocks);
   size_t o_bt = append_bytes(buf, P->btasks);
@@ -391,6 +395,7 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
     }
     const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : (o.host_only ? 3 : std::max(1, fp64_max_ctas_per_sm()));
     pm.parallel_ctas = P->sm_count * cps;
+    pm.sms = P->sm_count;
 
     const bool sorted_pack = true;
     auto packed = [&](const bs_layout &src, uint32_t mode, bs_layout *dst) {
@@ -628,7 +633,7 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
     p.groups = P->d_groups;
     p.rsegs = P->d_rsegs;
     p.ksegs = P->d_ksegs;
-    p.tail_groups = P->d_tail;
+    p.tail_elems = (const int2 *)P->d_tail;
     p.ntasks = (int32_t)P->ts.tasks.size();
     p.counter = P->d_counter;
     p.status = P->d_status;
@@ -636,13 +641,14 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
   } else {
     if (((uintptr_t)Ause | (uintptr_t)Buse | (uintptr_t)C) % 16 != 0) return BS_ERR_MISALIGNED;
     if (P->btasks.empty()) return BS_OK;
-    if (P->maps_a_ptr != Ause || P->maps_b_ptr != Buse) {
-      bs_status st = encode_maps(P, Ause, Buse);
+    if (P->maps_a_ptr != Ause || P->maps_b_ptr != Buse || P->maps_c_ptr != C) {
+      bs_status st = encode_maps(P, Ause, Buse, C);
       if (st != BS_OK) return st;
       BS_CUDA(cudaMemcpyAsync(P->d_maps, P->map_bytes.data(), P->map_bytes.size(), cudaMemcpyHostToDevice, s));
       BS_CUDA(cudaStreamSynchronize(s));
       P->maps_a_ptr = Ause;
       P->maps_b_ptr = Buse;
+      P->maps_c_ptr = C;
     }
     Bf16Params p{};
     p.maps = P->d_maps;

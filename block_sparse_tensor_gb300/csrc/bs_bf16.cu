@@ -15,7 +15,8 @@
 //           tile 64 x BN (N-major, 128-byte swizzle) per stage, 4 stages;
 //   warp 1  TMEM owner and MMA issuer (one thread): 4 x (M128, N=BN, K16) per
 //           stage into one of two 256-column FP32 accumulators;
-//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, masked stores.
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, staged through
+//           swizzled shared memory, TMA tensor stores clipped at the group edge.
 // Every wait is bounded by the global timer; on expiry the kernel records
 // a timeout in the status word, drains its copies and MMAs (again bounded),
 // frees its tensor memory and returns.
@@ -47,7 +48,11 @@ struct Ctl {
   int32_t abort_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)kStages * kStageBytes + sizeof(Ctl) + 64;
+constexpr int kCtlBytes = 256;                    // Ctl rounded up
+constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x 32 FP32 columns
+constexpr size_t kSmemBytes =
+    1024 /*align slack*/ + (size_t)kStages * kStageBytes + kCtlBytes + 4 * 2 * kEpiBufBytes;
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -148,7 +153,8 @@ __device__ __forceinline__ void record_timeout(const Bf16Params &p, Ctl *ctl) {
 __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf16Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  Ctl *ctl = (Ctl *)(smem + (size_t)kStages * kStageBytes);
+  // [stages | epilogue staging, 1024-aligned for the 128-byte swizzle | control block]
+  Ctl *ctl = (Ctl *)(smem + (size_t)kStages * kStageBytes + 4 * 2 * kEpiBufBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int32_t *abort_flag = &ctl->abort_flag;
 
@@ -296,9 +302,17 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;   // TMEM lanes 32*quarter .. 32*quarter+31
+    // Each warp owns TMEM lanes 32*quarter .. +31 (tile rows) and two 4 KB
+    // staging buffers.  A 32 x 32 FP32 chunk goes TMEM -> registers -> shared
+    // memory (128-byte swizzle, so the 32 row writes of one column group hit
+    // distinct banks) -> one TMA tensor store, which clips rows and columns
+    // past the group's edge.  Unaligned C views fall back to direct stores.
+    const int quarter = warp & 3;
+    unsigned char *stage_buf = smem + (size_t)kStages * kStageBytes + (size_t)quarter * 2 * kEpiBufBytes;
+    const char *maps = (const char *)p.maps;
     int acc = 0;
     uint32_t acc_phase = 0;
+    int buf = 0;
     for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
       const Bf16Task T = p.tasks[t];
       if (!mbar_wait(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, p.timeout_ns)) {
@@ -306,20 +320,40 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
         break;
       }
       fence_after();
-      const int row = T.m0 + quarter * 32 + lane;
-      const bool row_ok = row < T.m;
-      float *crow = p.C + T.c_off + (int64_t)row * T.ldc + T.n0;
-      const bool vec = ((T.c_off | T.ldc) & 3) == 0;
-      const int ncols = min(T.bn, T.n - T.n0);
-      for (int c0 = 0; c0 < T.bn; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * 256 + c0), v);
-        if (!row_ok) continue;
-        if (vec && c0 + 16 <= ncols) {
-          float4 *d = (float4 *)(crow + c0);
+      const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * 256);
+      if (T.map_c >= 0 && T.m0 + quarter * 32 < T.m) {   // quarters wholly past the last row store nothing
+        const void *mc = maps + (size_t)T.map_c * 128;
+        for (int c0 = 0; c0 < T.bn; c0 += 32) {
+          float v[32];
+          tmem_ld16(trow + c0, v);
+          tmem_ld16(trow + c0 + 16, v + 16);
+          // the buffer written two chunks ago must have been read by its store
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          __syncwarp();
+          unsigned char *b = stage_buf + buf * kEpiBufBytes + lane * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        } else {
+          for (int j = 0; j < 8; ++j)
+            *(float4 *)(b + ((j ^ (lane & 7)) << 4)) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            asm volatile(
+                "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(mc),
+                "r"(smem_u32(stage_buf + buf * kEpiBufBytes)), "r"(T.n0 + c0), "r"(T.m0 + quarter * 32)
+                : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+          buf ^= 1;
+        }
+      } else if (T.map_c < 0) {
+        const int row = T.m0 + quarter * 32 + lane;
+        const bool row_ok = row < T.m;
+        float *crow = p.C + T.c_off + (int64_t)row * T.ldc + T.n0;
+        const int ncols = min(T.bn, T.n - T.n0);
+        for (int c0 = 0; c0 < T.bn; c0 += 16) {
+          float v[16];
+          tmem_ld16(trow + c0, v);
+          if (!row_ok) continue;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (c0 + i < ncols) crow[c0 + i] = v[i];
@@ -333,6 +367,9 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
         acc_phase ^= 1u;
       }
     }
+    // staged stores finish reading shared memory before the CTA can exit
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
   }
   fence_before();
   __syncthreads();

@@ -11,8 +11,12 @@
 //     per-row and per-k address tables, so inner blocks of any size and any
 //     number of views cost no padding flops.  Outputs are spread one per
 //     thread slot, so a tile of any shape keeps the FP64 lanes busy.
-//   - TAIL: up to eight tiny groups (at most 64 outputs each), one warp per
-//     group, accumulating in registers straight from the L1-cached operands.
+//   - TAIL: small groups (at most 4096 outputs each) with one output per
+//     thread, outputs of consecutive groups packed lane after lane so that no
+//     FMA is issued for an idle lane, accumulating in registers straight from
+//     the L1-cached operands.  Idle lanes of a warp cost the FP64 pipe as much
+//     as busy ones on this part, which is why outputs, not groups, are spread
+//     over the lanes.
 // Stores are plain for contraction-axis groups (each C block has one writer)
 // and atomic adds for free-axis groups (several k add into one C block).
 #include "bs_host.h"
@@ -118,62 +122,54 @@ __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
   }
 }
 
+// One output per thread.  The loop count is the warp's longest K; a lane whose
+// group is shorter stops adding.  Segment changes are per-lane branches; the
+// FMA itself is issued once per iteration for the whole warp.
 __device__ void run_tail(const Fp64Params &p, const Task &T) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp >= T.m0) return;
-  const Group G = p.groups[p.tail_groups[T.g + warp]];
+  const int tid = threadIdx.x;
+  const bool ok = tid < T.m0;
+  int2 el = make_int2(0, 0);
+  if (ok) el = p.tail_elems[T.g + tid];
+  const Group G = p.groups[el.x];
+  const int r = el.y >> 16, c = el.y & 0xFFFF;
+  const int kg = ok ? G.k : 0;
+  const int kmax = __reduce_max_sync(0xFFFFFFFFu, (unsigned)kg);
+  if (kmax == 0) return;
   const RowSeg *rs = p.rsegs + G.rseg_begin;
   const KSeg *ks = p.ksegs + G.kseg_begin;
-  const int ne = G.m * G.n;
-  // two outputs per lane (tiny groups hold at most 64)
-  int64_t ra[2], rl[2], rc[2];
-  int col[2];
-  bool ok[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int e = lane + 32 * u;
-    ok[u] = e < ne;
-    const int r = ok[u] ? e / G.n : 0;
-    col[u] = ok[u] ? e - r * G.n : 0;
-    const RowSeg s = rs[find_rseg(rs, G.rseg_count, r)];
-    const int64_t lr = r - s.r0;
-    ra[u] = s.ra + lr * s.lda;
-    rl[u] = s.rl ? lr : 0;
-    rc[u] = s.rc + lr * s.ldc;
-  }
-  double acc0 = 0.0, acc1 = 0.0;
-  for (int si = 0; si < G.kseg_count; ++si) {
-    const KSeg s = ks[si];
-    const double *a0 = p.A + ra[0] + s.ka + rl[0] * s.kl;
-    const double *a1 = p.A + ra[1] + s.ka + rl[1] * s.kl;
-    const double *b0 = p.B + s.kb + col[0];
-    const double *b1 = p.B + s.kb + col[1];
-    const int64_t ldb = s.ldb;
-    if (ok[1]) {
-#pragma unroll 4
-      for (int q = 0; q < s.klen; ++q) {
-        acc0 = fma(__ldg(a0 + q), __ldg(b0 + q * ldb), acc0);
-        acc1 = fma(__ldg(a1 + q), __ldg(b1 + q * ldb), acc1);
+  const RowSeg s = rs[ok ? find_rseg(rs, G.rseg_count, r) : 0];
+  const int64_t lr = r - s.r0;
+  const int64_t ra = s.ra + lr * s.lda, rl = s.rl ? lr : 0;
+  int si = 0;
+  KSeg k = ks[0];
+  const double *ap = p.A + ra + k.ka + rl * k.kl;
+  const double *bp = p.B + k.kb + c;
+  int64_t ldb = k.ldb;
+  int rem = k.klen;
+  double acc = 0.0;
+  for (int it = 0; it < kmax; ++it) {
+    if (it < kg) {
+      if (rem == 0) {
+        k = ks[++si];
+        ap = p.A + ra + k.ka + rl * k.kl;
+        bp = p.B + k.kb + c;
+        ldb = k.ldb;
+        rem = k.klen;
       }
-    } else if (ok[0]) {
-#pragma unroll 4
-      for (int q = 0; q < s.klen; ++q) acc0 = fma(__ldg(a0 + q), __ldg(b0 + q * ldb), acc0);
+      acc = fma(__ldg(ap), __ldg(bp), acc);
+      ++ap;
+      bp += ldb;
+      --rem;
     }
   }
-  const bool atomic = (G.flags & GF_ATOMIC) != 0;
-  if (ok[0]) {
-    double *d = p.C + rc[0] + col[0];
-    if (atomic) atomicAdd(d, acc0);
-    else *d = acc0;
-  }
-  if (ok[1]) {
-    double *d = p.C + rc[1] + col[1];
-    if (atomic) atomicAdd(d, acc1);
-    else *d = acc1;
+  if (ok) {
+    double *d = p.C + s.rc + lr * s.ldc + c;
+    if (G.flags & GF_ATOMIC) atomicAdd(d, acc);
+    else *d = acc;
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 3) fp64_grouped_kernel(Fp64Params p) {
+__global__ void __launch_bounds__(kThreads, 4) fp64_grouped_kernel(Fp64Params p) {
   __shared__ TileSmem sm;
   for (;;) {
     if (threadIdx.x == 0) sm.task = (int)atomicAdd(&p.counter[0], 1u);

@@ -22,6 +22,7 @@
 // segment {ka 0, kl 0, kb b_off, ldb}; its stores are atomic adds.
 #pragma once
 #include <stdint.h>
+#include <vector_types.h>
 
 namespace bs {
 
@@ -57,11 +58,14 @@ struct Group {
 enum TaskKind : int32_t { TK_TILE = 0, TK_TAIL = 1 };
 
 // TK_TILE: one CTA computes rows m0 .. m0+tm-1, columns n0 .. n0+tn-1 of group `g`.
-// TK_TAIL: one CTA runs up to kTailPerTask tiny groups, one warp each; their
-//          ids are tail_groups[first .. first+count-1].
+// TK_TAIL: one CTA computes up to kThreads outputs of small groups, one output
+//          per thread: thread t takes tail_elems[first + t] = {group, r << 16 | c}.
+//          Outputs are listed group after group with the groups in decreasing
+//          K, so the lanes of one warp run loops of nearly equal length and
+//          every FMA instruction carries (almost) 32 useful lanes.
 struct Task {
   int32_t kind;
-  int32_t g;       // group (TILE) or first index into tail_groups (TAIL)
+  int32_t g;       // group (TILE) or first index into tail_elems (TAIL)
   int32_t m0;      // (TILE) or count (TAIL)
   int32_t n0;
   int32_t tm;
@@ -73,8 +77,7 @@ constexpr int kElemsPerThread = 4;     // tile outputs per thread
 constexpr int kTileMaxElems = kThreads * kElemsPerThread;
 constexpr int kTileMaxDim = 128;       // bound on tm and tn
 constexpr int kKC = 16;                // inner chunk per shared-memory stage
-constexpr int kTailPerTask = kThreads / 32;
-constexpr int kTailMaxElems = 64;      // a group this small runs on one warp
+constexpr int kTailMaxElems = 4096;    // groups up to this many outputs take the lane-packed path
 
 // One block copy of the gather ("pack") kernel.
 struct PackCopy {
@@ -105,7 +108,7 @@ struct Fp64Params {
   const Group *groups;
   const RowSeg *rsegs;
   const KSeg *ksegs;
-  const int32_t *tail_groups;
+  const int2 *tail_elems;
   int32_t ntasks;
   int32_t pad_;
   uint32_t *counter;   // [0] next task, [1] CTAs finished; both return to 0 at exit
@@ -139,7 +142,7 @@ struct Bf16Task {
   int32_t m;         // rows of the group
   int32_t n;         // columns of the group
   int32_t bn;        // UMMA N of the tile (multiple of 16, <= 256)
-  int32_t pad_;
+  int32_t map_c;     // tensor map of the group's C view, or -1 for direct stores
   int64_t c_off;     // C offset of the group's (0, 0) element
   int64_t ldc;
 };

@@ -282,18 +282,22 @@ void group_triples(const GroupSet &gs, std::vector<int64_t> *ptr, std::vector<in
 
 // ---- FP64 tiling -----------------------------------------------------------
 
-static void tile_shape(int32_t m, int32_t n, int32_t *tm, int32_t *tn) {
-  // Outputs are spread one per thread-slot, so any tm x tn <= kTileMaxElems keeps
-  // every lane busy; the shape only has to follow the group's aspect ratio.
+// Outputs are spread one per thread slot, so any tm x tn <= kTileMaxElems keeps
+// the lanes busy; the shape follows the group's aspect ratio and its area is
+// capped so that no single task outlasts the rest of the launch.
+static void tile_shape(int32_t m, int32_t n, int32_t area, int32_t *tm, int32_t *tn) {
+  area = std::max(32, std::min(area, kTileMaxElems));
   if (n <= 8) {
     *tn = n;
-    *tm = std::min(m, std::min(kTileMaxDim, kTileMaxElems / n));
+    *tm = std::min(m, std::min(kTileMaxDim, std::max(1, area / n)));
   } else if (m <= 8) {
     *tm = m;
-    *tn = std::min(n, std::min(kTileMaxDim, kTileMaxElems / m));
+    *tn = std::min(n, std::min(kTileMaxDim, std::max(1, area / m)));
   } else {
-    *tn = std::min(n, 32);
-    *tm = std::min(m, std::min(kTileMaxDim, kTileMaxElems / *tn));
+    int32_t side = 8;
+    while (side * 2 * side * 2 <= area && side < 32) side *= 2;
+    *tn = std::min(n, side);
+    *tm = std::min(m, std::min(kTileMaxDim, std::max(1, area / *tn)));
   }
 }
 
@@ -301,20 +305,22 @@ static inline int64_t lanes(int64_t e) { return (e + 31) / 32 * 32; }
 
 void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
   ts->tasks.clear();
-  ts->tail_groups.clear();
+  ts->tail_elems.clear();
   std::vector<std::pair<double, Task>> costed;
   std::vector<int32_t> tails;
-  double exec = 0;
+  double exec = 0, work = 0;
+  for (const auto &G : gs.groups) work += (double)G.m * G.n * G.k;
+  // per-task work target: a few tasks per SM, so longest-first scheduling balances
+  const double target = std::max(8192.0, work / (std::max(1, pm.sms) * 4.0));
   for (int32_t g = 0; g < (int32_t)gs.groups.size(); ++g) {
     const Group &G = gs.groups[g];
     const int64_t e = (int64_t)G.m * G.n;
     if (e <= kTailMaxElems) {
       tails.push_back(g);
-      exec += 2.0 * lanes(e) * G.k;
       continue;
     }
     int32_t tm, tn;
-    tile_shape(G.m, G.n, &tm, &tn);
+    tile_shape(G.m, G.n, (int32_t)std::min<double>(kTileMaxElems, target / std::max(1, G.k)), &tm, &tn);
     for (int32_t m0 = 0; m0 < G.m; m0 += tm)
       for (int32_t n0 = 0; n0 < G.n; n0 += tn) {
         Task t{};
@@ -329,22 +335,31 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
         costed.push_back({slots * G.k + pm.task_slots, t});
       }
   }
-  // tiny groups: longest K first, bundled kTailPerTask at a time so the warps
-  // of one bundle finish together
+  // Small groups: every output gets its own lane.  Groups are ordered by
+  // decreasing K so that the 32 lanes of a warp run loops of nearly equal
+  // length; a task is kThreads consecutive outputs.
   std::stable_sort(tails.begin(), tails.end(),
                    [&](int32_t a, int32_t b) { return gs.groups[a].k > gs.groups[b].k; });
-  ts->tail_groups = tails;
-  for (size_t f = 0; f < tails.size(); f += kTailPerTask) {
+  std::vector<int32_t> elem_k;
+  for (int32_t g : tails) {
+    const Group &G = gs.groups[g];
+    for (int32_t r = 0; r < G.m; ++r)
+      for (int32_t c = 0; c < G.n; ++c) {
+        ts->tail_elems.push_back(g);
+        ts->tail_elems.push_back((r << 16) | c);
+        elem_k.push_back(G.k);
+      }
+  }
+  const size_t ne = elem_k.size();
+  for (size_t f = 0; f < ne; f += kThreads) {
     Task t{};
     t.kind = TK_TAIL;
     t.g = (int32_t)f;
-    t.m0 = (int32_t)std::min<size_t>(kTailPerTask, tails.size() - f);
-    double c = 0;
-    for (int32_t u = 0; u < t.m0; ++u) {
-      const Group &G = gs.groups[tails[f + u]];
-      c = std::max(c, (double)lanes((int64_t)G.m * G.n) * G.k);
-    }
-    costed.push_back({c * kTailPerTask / 2 + pm.task_slots, t});
+    t.m0 = (int32_t)std::min<size_t>(kThreads, ne - f);
+    double slots = 0;
+    for (size_t w = f; w < f + t.m0; w += 32) slots += 32.0 * elem_k[w];   // first lane holds the warp's longest K
+    exec += 2.0 * slots;
+    costed.push_back({slots + pm.task_slots, t});
   }
   // longest processing time first for the dynamic scheduler
   std::stable_sort(costed.begin(), costed.end(),

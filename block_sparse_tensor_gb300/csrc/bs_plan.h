@@ -20,7 +20,7 @@ struct GroupSet {
 
 struct TileSet {
   std::vector<Task> tasks;
-  std::vector<int32_t> tail_groups;
+  std::vector<int32_t> tail_elems;   // pairs: group, r << 16 | c
   double executed_flops = 0;
 };
 
@@ -33,6 +33,7 @@ struct PlanModel {
   double atomic_penalty = 0.5;
   double task_slots = 4096;   // LPT weight of a task's fixed cost, in lane-flop units
   int parallel_ctas = 456;
+  int sms = 152;
 };
 
 GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C, bool merge_rows,
@@ -46,7 +47,7 @@ double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm,
 // Host description of one TMA tensor map of the BF16 path (encoded per call
 // with the caller's base pointer, then cached while the pointers stay the same).
 struct MapDesc {
-  int32_t operand;      // 0: A, 1: B
+  int32_t operand;      // 0: A, 1: B, 2: C (FP32)
   int64_t off;          // element offset of the view's first element
   int64_t inner;        // contiguous extent (elements)
   int64_t outer;        // rows
@@ -74,7 +75,7 @@ struct bs_plan {
   std::vector<bs::Bf16Pair> bpairs;
   std::vector<bs::MapDesc> maps;
   std::vector<unsigned char> map_bytes;   // encoded maps (128 bytes each)
-  const void *maps_a_ptr = nullptr, *maps_b_ptr = nullptr;
+  const void *maps_a_ptr = nullptr, *maps_b_ptr = nullptr, *maps_c_ptr = nullptr;
   // device state
   int device = -1;
   int sm_count = 0;

@@ -246,6 +246,22 @@ void bs_plan_destroy(bs_plan *plan);
 
 const char *bs_status_string(bs_status status);
 
+/* Cost-model constants measured on the current device.  The design note
+ * "block coalescing" ("The crossover decides whether to coalesce") takes its
+ * launch cost and flop rate from calibrated constants that the pages do not
+ * print; this call measures them with small probe kernels on `stream`
+ * (allocating and freeing about 2 GiB of scratch) and synchronizes. */
+typedef struct bs_calibration {
+  double fp64_gflops;               /* FP64 FMA rate, every lane of every warp active */
+  double fp64_gflops_quarter_warp;  /* the same with 8 of 32 lanes active (useful flops) */
+  double launch_us;                 /* back-to-back empty-kernel launch interval */
+  double copy_gbs;                  /* device copy bandwidth, read + write bytes */
+  int32_t sm_count;
+  int32_t reserved[7];
+} bs_calibration;
+
+bs_status bs_calibrate(bs_calibration *out, void *stream);
+
 /* Library build identification, e.g. "bs 0.1 sm_103a". */
 const char *bs_version(void);
 
