@@ -523,8 +523,9 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
     const int eb_out = dtype == BS_F64 ? 8 : 4;
     S.useful_bytes = (double)(populated_elems(P->A) + populated_elems(P->B)) * eb_in + (double)populated_elems(P->C) * eb_out;
     if (dtype == BS_F64) {
-      S.tasks = (int64_t)P->ts.tasks.size();
-      for (const auto &t : P->ts.tasks) (t.kind == TK_TILE ? S.tile_tasks : S.tail_tasks)++;
+      S.tile_tasks = (int64_t)P->ts.tasks.size();
+      S.tail_tasks = (int64_t)(P->ts.tail_elems.size() / 2 + 31) / 32;   // warp-sized pieces of the tail list
+      S.tasks = S.tile_tasks + S.tail_tasks;
       S.executed_flops = P->ts.executed_flops;
     } else {
       S.tasks = S.tile_tasks = (int64_t)P->btasks.size();
@@ -545,7 +546,10 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
         delete P;
         return st;
       }
-      if (dtype == BS_F64) P->grid = std::max(1, std::min<int>((int)P->ts.tasks.size(), P->sm_count * cps));
+      if (dtype == BS_F64) {
+        const int64_t work_items = (int64_t)P->ts.tasks.size() + (int64_t)(P->ts.tail_elems.size() / 2 + kThreads - 1) / kThreads;
+        P->grid = (int)std::max<int64_t>(1, std::min<int64_t>(work_items, (int64_t)P->sm_count * cps));
+      }
       else P->grid = std::max(1, std::min<int>((int)P->btasks.size(), P->sm_count));
     }
   } catch (const std::bad_alloc &) {
@@ -624,7 +628,7 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
   if (!P->zero_blocks.empty())
     BS_CUDA(launch_zero(C, P->dtype == BS_F64 ? 8 : 4, P->d_zero, (int)P->zero_blocks.size(), P->sm_count * 4, s));
   if (P->dtype == BS_F64) {
-    if (P->ts.tasks.empty()) return BS_OK;
+    if (P->ts.tasks.empty() && P->ts.tail_elems.empty()) return BS_OK;
     Fp64Params p{};
     p.A = (const double *)Ause;
     p.B = (const double *)Buse;
@@ -635,6 +639,7 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
     p.ksegs = P->d_ksegs;
     p.tail_elems = (const int2 *)P->d_tail;
     p.ntasks = (int32_t)P->ts.tasks.size();
+    p.ntail = (int32_t)(P->ts.tail_elems.size() / 2);
     p.counter = P->d_counter;
     p.status = P->d_status;
     BS_CUDA(launch_fp64_grouped(p, P->grid, s));

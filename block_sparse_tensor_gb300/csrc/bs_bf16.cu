@@ -98,6 +98,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile 
   }
 }
 
+__device__ __forceinline__ void prefetch_map(const void *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// Warm the descriptor cache with every tensor map task `t` will use.
+__device__ __forceinline__ void prefetch_task_maps(const Bf16Params &p, const char *maps, int t) {
+  if (t >= p.ntasks) return;
+  const Bf16Task T = p.tasks[t];
+  for (int q = 0; q < T.pair_count; ++q) {
+    const Bf16Pair pr = p.pairs[T.pair_begin + q];
+    prefetch_map(maps + (size_t)pr.map_a * 128);
+    prefetch_map(maps + (size_t)pr.map_b * 128);
+  }
+  if (T.map_c >= 0) prefetch_map(maps + (size_t)T.map_c * 128);
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint32_t mbar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
@@ -193,8 +209,10 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       uint32_t issued_phase[kStages];
       bool outstanding[kStages];
       for (int s = 0; s < kStages; ++s) outstanding[s] = false;
+      prefetch_task_maps(p, maps, blockIdx.x);
       for (int t = blockIdx.x; ok && t < p.ntasks; t += gridDim.x) {
         const Bf16Task T = p.tasks[t];
+        prefetch_task_maps(p, maps, t + gridDim.x);   // the next task's descriptors load while this one streams
         const int nb = (T.bn + 63) / 64;
         const uint32_t bytes = kATileBytes + nb * kBChunkBytes;
         for (int q = 0; ok && q < T.pair_count; ++q) {

@@ -122,44 +122,55 @@ __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
   }
 }
 
-// One output per thread.  The loop count is the warp's longest K; a lane whose
-// group is shorter stops adding.  Segment changes are per-lane branches; the
-// FMA itself is issued once per iteration for the whole warp.
-__device__ void run_tail(const Fp64Params &p, const Task &T) {
-  const int tid = threadIdx.x;
-  const bool ok = tid < T.m0;
-  int2 el = make_int2(0, 0);
-  if (ok) el = p.tail_elems[T.g + tid];
+// One output per lane for 32 consecutive outputs of the tail list.  The loop
+// count is the warp's longest K; a lane whose group is shorter stops adding.
+// When every lane's group is one view (the usual case with panel layouts) the
+// loop is unrolled with two accumulators; otherwise each lane walks its
+// group's views, switching view on its own.
+__device__ void run_tail_warp(const Fp64Params &p, int w) {
+  const int lane = threadIdx.x & 31;
+  const int e = w * 32 + lane;
+  const bool ok = e < p.ntail;
+  const int2 el = ok ? p.tail_elems[e] : make_int2(p.tail_elems[w * 32].x, 0);
   const Group G = p.groups[el.x];
   const int r = el.y >> 16, c = el.y & 0xFFFF;
   const int kg = ok ? G.k : 0;
   const int kmax = __reduce_max_sync(0xFFFFFFFFu, (unsigned)kg);
-  if (kmax == 0) return;
   const RowSeg *rs = p.rsegs + G.rseg_begin;
   const KSeg *ks = p.ksegs + G.kseg_begin;
-  const RowSeg s = rs[ok ? find_rseg(rs, G.rseg_count, r) : 0];
+  const RowSeg s = rs[find_rseg(rs, G.rseg_count, r)];
   const int64_t lr = r - s.r0;
   const int64_t ra = s.ra + lr * s.lda, rl = s.rl ? lr : 0;
-  int si = 0;
   KSeg k = ks[0];
   const double *ap = p.A + ra + k.ka + rl * k.kl;
   const double *bp = p.B + k.kb + c;
   int64_t ldb = k.ldb;
-  int rem = k.klen;
   double acc = 0.0;
-  for (int it = 0; it < kmax; ++it) {
-    if (it < kg) {
-      if (rem == 0) {
-        k = ks[++si];
-        ap = p.A + ra + k.ka + rl * k.kl;
-        bp = p.B + k.kb + c;
-        ldb = k.ldb;
-        rem = k.klen;
+  if (__all_sync(0xFFFFFFFFu, G.kseg_count == 1)) {
+    double acc1 = 0.0;
+    int it = 0;
+    for (; it + 2 <= kmax; it += 2) {
+      if (it < kg) acc = fma(__ldg(ap + it), __ldg(bp + it * ldb), acc);
+      if (it + 1 < kg) acc1 = fma(__ldg(ap + it + 1), __ldg(bp + (it + 1) * ldb), acc1);
+    }
+    if (it < kg) acc = fma(__ldg(ap + it), __ldg(bp + it * ldb), acc);
+    acc += acc1;
+  } else {
+    int si = 0, rem = k.klen;
+    for (int it = 0; it < kmax; ++it) {
+      if (it < kg) {
+        if (rem == 0) {
+          k = ks[++si];
+          ap = p.A + ra + k.ka + rl * k.kl;
+          bp = p.B + k.kb + c;
+          ldb = k.ldb;
+          rem = k.klen;
+        }
+        acc = fma(__ldg(ap), __ldg(bp), acc);
+        ++ap;
+        bp += ldb;
+        --rem;
       }
-      acc = fma(__ldg(ap), __ldg(bp), acc);
-      ++ap;
-      bp += ldb;
-      --rem;
     }
   }
   if (ok) {
@@ -171,23 +182,33 @@ __device__ void run_tail(const Fp64Params &p, const Task &T) {
 
 __global__ void __launch_bounds__(kThreads, 4) fp64_grouped_kernel(Fp64Params p) {
   __shared__ TileSmem sm;
+  // tile tasks, one CTA each, longest first
   for (;;) {
     if (threadIdx.x == 0) sm.task = (int)atomicAdd(&p.counter[0], 1u);
     __syncthreads();
     const int t = sm.task;
     __syncthreads();
     if (t >= p.ntasks) break;
-    const Task T = p.tasks[t];
-    if (T.kind == TK_TILE) run_tile(p, T, sm);
-    else run_tail(p, T);
+    run_tile(p, p.tasks[t], sm);
   }
-  // The last CTA to leave returns both counters to zero for the next launch.
-  // Every CTA has taken its final task index before it counts itself out.
+  // then the tail list, 32 outputs per warp at a time
+  const int ntw = (p.ntail + 31) / 32;
+  for (;;) {
+    int w = 0;
+    if ((threadIdx.x & 31) == 0) w = (int)atomicAdd(&p.counter[2], 1u);
+    w = __shfl_sync(0xFFFFFFFFu, w, 0);
+    if (w >= ntw) break;
+    run_tail_warp(p, w);
+  }
+  __syncthreads();
+  // The last CTA to leave returns the counters to zero for the next launch.
+  // Every CTA has taken its final work index before it counts itself out.
   if (threadIdx.x == 0) {
     __threadfence();
     const unsigned prev = atomicAdd(&p.counter[1], 1u);
     if (prev == gridDim.x - 1) {
       atomicExch(&p.counter[0], 0u);
+      atomicExch(&p.counter[2], 0u);
       atomicExch(&p.counter[1], 0u);
     }
   }

@@ -55,18 +55,18 @@ struct Group {
   int32_t kseg_begin, kseg_count;
 };
 
-enum TaskKind : int32_t { TK_TILE = 0, TK_TAIL = 1 };
+enum TaskKind : int32_t { TK_TILE = 0 };
 
 // TK_TILE: one CTA computes rows m0 .. m0+tm-1, columns n0 .. n0+tn-1 of group `g`.
-// TK_TAIL: one CTA computes up to kThreads outputs of small groups, one output
-//          per thread: thread t takes tail_elems[first + t] = {group, r << 16 | c}.
-//          Outputs are listed group after group with the groups in decreasing
-//          K, so the lanes of one warp run loops of nearly equal length and
-//          every FMA instruction carries (almost) 32 useful lanes.
+// Small groups are not tasks: their outputs form the tail list
+// tail_elems[e] = {group, r << 16 | c}, groups in decreasing K, and each warp
+// takes 32 consecutive outputs at a time (one per lane) once the tile tasks
+// are all taken, so the lanes of one warp run loops of nearly equal length
+// and every FMA instruction carries (almost) 32 useful lanes.
 struct Task {
   int32_t kind;
-  int32_t g;       // group (TILE) or first index into tail_elems (TAIL)
-  int32_t m0;      // (TILE) or count (TAIL)
+  int32_t g;       // group
+  int32_t m0;
   int32_t n0;
   int32_t tm;
   int32_t tn;
@@ -110,8 +110,8 @@ struct Fp64Params {
   const KSeg *ksegs;
   const int2 *tail_elems;
   int32_t ntasks;
-  int32_t pad_;
-  uint32_t *counter;   // [0] next task, [1] CTAs finished; both return to 0 at exit
+  int32_t ntail;       // outputs in the tail list
+  uint32_t *counter;   // [0] next tile task, [1] CTAs finished, [2] next tail warp; all return to 0
   int32_t *status;
 };
 

@@ -337,7 +337,7 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
   }
   // Small groups: every output gets its own lane.  Groups are ordered by
   // decreasing K so that the 32 lanes of a warp run loops of nearly equal
-  // length; a task is kThreads consecutive outputs.
+  // length; warps take 32 consecutive outputs at a time.
   std::stable_sort(tails.begin(), tails.end(),
                    [&](int32_t a, int32_t b) { return gs.groups[a].k > gs.groups[b].k; });
   std::vector<int32_t> elem_k;
@@ -350,17 +350,7 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
         elem_k.push_back(G.k);
       }
   }
-  const size_t ne = elem_k.size();
-  for (size_t f = 0; f < ne; f += kThreads) {
-    Task t{};
-    t.kind = TK_TAIL;
-    t.g = (int32_t)f;
-    t.m0 = (int32_t)std::min<size_t>(kThreads, ne - f);
-    double slots = 0;
-    for (size_t w = f; w < f + t.m0; w += 32) slots += 32.0 * elem_k[w];   // first lane holds the warp's longest K
-    exec += 2.0 * slots;
-    costed.push_back({slots + pm.task_slots, t});
-  }
+  for (size_t w = 0; w < elem_k.size(); w += 32) exec += 2.0 * 32.0 * elem_k[w];   // lane 0 holds the warp's longest K
   // longest processing time first for the dynamic scheduler
   std::stable_sort(costed.begin(), costed.end(),
                    [](const std::pair<double, Task> &a, const std::pair<double, Task> &b) { return a.first > b.first; });

@@ -143,19 +143,46 @@ def test_single_sector_is_a_dense_gemm(mkn, dtype):
     compare(r, r.run())
 
 
-def test_poisoned_c_only_populated_elements_written():
-    """C starts as NaN: every populated element is written, padding keeps its NaN."""
+def _poison_check(r, c, granule_elems):
+    """Populated elements are all written; padding keeps its NaN, except (BF16 path)
+    the padding inside the 16-byte granule that holds a block row's last element,
+    which the copy engine's granule-wide stores set to exactly zero."""
+    from harness import element_index
+    blocks = r.P.c_layout.blocks()
+    idx = np.zeros(r.P.c_layout.nelems, bool)
+    idx[element_index(blocks)] = True
+    assert not np.any(np.isnan(c[idx]))
+    pad = ~idx
+    assert pad.sum() > 0
+    allowed = np.zeros_like(pad)
+    if granule_elems > 1:
+        for (_, _, off, nr, nc, ld) in blocks:
+            ends = off + np.arange(nr) * ld + nc                   # first element after each row
+            granule_end = ((ends - 1) // granule_elems + 1) * granule_elems
+            for e in range(granule_elems - 1):
+                pos = ends + e
+                allowed[pos[pos < granule_end]] = True
+    assert np.all(np.isnan(c[pad & ~allowed])), "padding outside the last granule of a row was written"
+    assert np.all(np.isnan(c[pad & allowed]) | (c[pad & allowed] == 0.0))
+
+
+def test_poisoned_c_bf16_only_populated_elements_and_granule_padding_written():
     w = bsgen.config4()
     w.rows, w.inner, w.cols = (bsgen.Axis(a.q[:40], a.d[:40]) if a.n == 100 else bsgen.Axis(a.q[:10], a.d[:10])
                                for a in (w.rows, w.inner, w.cols))
     r = Run(w)
     c = r.run()
-    idx = np.zeros(r.P.c_layout.nelems, bool)
-    from harness import element_index
-    idx[element_index(r.P.c_layout.blocks())] = True
-    assert not np.any(np.isnan(c[idx]))
-    assert np.all(np.isnan(c[~idx])) and (~idx).sum() > 0
+    _poison_check(r, c, granule_elems=4)
     compare(r, c)
+
+
+def test_poisoned_c_fp64_padding_untouched():
+    w = bsgen.config2()
+    for pol in ("contraction", "free", "none"):
+        r = Run(w, "rowpanel|charge_sorted", "colpanel|charge_sorted", "rowpanel|align16", **POLICIES[pol])
+        c = r.run()
+        _poison_check(r, c, granule_elems=1)
+        compare(r, c)
 
 
 def test_repeated_calls_are_identical():
