@@ -31,7 +31,7 @@ EXPORTED = ["bs_layout_create", "bs_layout_query", "bs_layout_blocks", "bs_layou
             "bs_plan_options_default", "bs_plan_create", "bs_plan_c_layout", "bs_plan_stats_get",
             "bs_plan_groups", "bs_plan_triples", "bs_contract", "bs_contract_host",
             "bs_contract_uncoalesced", "bs_plan_last_device_error", "bs_plan_destroy",
-            "bs_status_string", "bs_version", "bs_calibrate"]
+            "bs_status_string", "bs_version", "bs_calibrate", "bs_contract_noalloc"]
 
 
 class BsError(RuntimeError):
@@ -106,6 +106,7 @@ def _load():
         "bs_status_string": (ctypes.c_char_p, [st]),
         "bs_version": (ctypes.c_char_p, []),
         "bs_calibrate": (st, [P, P]),
+        "bs_contract_noalloc": (st, [P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -288,6 +289,15 @@ def contract_uncoalesced(plan: Plan, A, B, C, stream=None):
     """The one-launch-per-triple control."""
     _check(lib.bs_contract_uncoalesced(plan.h, _ptr(A), _ptr(B), _ptr(C), _stream(stream)),
            "bs_contract_uncoalesced")
+
+
+def contract_noalloc(plan: Plan, A, B, C, stream=None):
+    """C = A B without any device allocation (FP64 plans; the plan may be host_only).
+
+    For callers that cannot allocate device memory: the plan's tables and
+    workspace go into a fixed 16 MiB device array inside the library, shared by
+    every call, so calls must not overlap on the GPU."""
+    _check(lib.bs_contract_noalloc(plan.h, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "bs_contract_noalloc")
 
 
 def last_device_error(plan: Plan, stream=None) -> int:

@@ -241,6 +241,27 @@ bs_status bs_contract_host(bs_plan *plan, const void *A_host, const void *B_host
  * (design note "block coalescing", Summary: tiny GEMMs are launch-bound). */
 bs_status bs_contract_uncoalesced(bs_plan *plan, const void *A, const void *B, void *C, void *stream);
 
+/* The FP64 contraction without any device allocation.  The design note has no
+ * counterpart to this call; it exists for callers that cannot call cudaMalloc
+ * (code running under a memory manager that owns all device memory, or a
+ * steady-state loop that must not allocate after start-up).  It does what
+ * bs_contract does, but the task tables, work counters and gather workspace
+ * live in one fixed device array of BS_NOALLOC_SCRATCH_BYTES inside the
+ * library (held on every device that loads the library until the process
+ * exits), so the plan may be built with host_only = 1 and nothing is allocated
+ * on the device, by this call or by the plan.  Each call copies the plan's
+ * tables into the array and zeroes its counters, on `stream`.
+ *   - FP64 plans only (UNSUPPORTED otherwise).
+ *   - A plan whose tables and workspace exceed the array returns OVERFLOW
+ *     before anything is enqueued.
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture begins.
+ *   - Every call shares the one array: calls that overlap on the GPU (other
+ *     streams, other host threads) race; order them on one stream.
+ *   - The FP64 kernel has no device waits, so there is no device status to read. */
+#define BS_NOALLOC_SCRATCH_BYTES (16u << 20)
+bs_status bs_contract_noalloc(const bs_plan *plan, const void *A, const void *B, void *C, void *stream);
+
 /* Synchronize `stream`, read and clear the plan's device status word.
  * Returns BS_OK, or the error a kernel recorded (TIMEOUT, DEVICE, ...). */
 bs_status bs_plan_last_device_error(bs_plan *plan, void *stream);
