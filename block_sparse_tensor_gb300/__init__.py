@@ -81,10 +81,10 @@ class Calibration(ctypes.Structure):
                 ("reserved", ctypes.c_int32 * 7)]
 
 
-def _load():
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libbs.so is not built ({LIB_PATH}); run block_sparse_tensor_gb300.build.build()")
-    L = ctypes.CDLL(LIB_PATH)
+def _load(path: str = LIB_PATH):
+    if not os.path.exists(path):
+        raise ImportError(f"libbs.so is not built ({path}); run block_sparse_tensor_gb300.build.build()")
+    L = ctypes.CDLL(path)
     P, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
     st = ctypes.c_int
     sig = {

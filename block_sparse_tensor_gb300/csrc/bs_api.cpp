@@ -212,6 +212,8 @@ bs_status upload(bs_plan *P) {
   size_t o_rsegs = append_bytes(buf, P->gs.rsegs);
   size_t o_ksegs = append_bytes(buf, P->gs.ksegs);
   size_t o_tail = append_bytes(buf, P->ts.tail_elems);
+  size_t o_tqp = append_bytes(buf, P->ts.tq_ptr);
+  size_t o_tqi = append_bytes(buf, P->ts.tq_items);
   size_t o_pack = append_bytes(buf, P->pack_copies);
   size_t o_zero = append_bytes(buf, P->zero_blocks);
   size_t o_bt = append_bytes(buf, P->btasks);
@@ -229,6 +231,8 @@ bs_status upload(bs_plan *P) {
   P->d_rsegs = (RowSeg *)(b + o_rsegs);
   P->d_ksegs = (KSeg *)(b + o_ksegs);
   P->d_tail = (int32_t *)(b + o_tail);
+  P->d_tq_ptr = (int32_t *)(b + o_tqp);
+  P->d_tq_items = (int32_t *)(b + o_tqi);
   P->d_pack = (PackCopy *)(b + o_pack);
   P->d_zero = (ZeroBlock *)(b + o_zero);
   P->d_btasks = (Bf16Task *)(b + o_bt);
@@ -236,8 +240,9 @@ bs_status upload(bs_plan *P) {
   P->d_maps = (void *)(b + o_maps);
   // counters and status word: zero once, kernels return them to zero
   void *cs = nullptr;
-  BS_CUDA(cudaMalloc(&cs, 256));
-  BS_CUDA(cudaMemset(cs, 0, 256));
+  P->counter_bytes = counter_bytes((int)std::max<size_t>(1, P->ts.tq_ptr.size()) - 1);
+  BS_CUDA(cudaMalloc(&cs, P->counter_bytes));
+  BS_CUDA(cudaMemset(cs, 0, P->counter_bytes));
   P->d_counter = (uint32_t *)cs;
   P->d_status = (int32_t *)((char *)cs + 128);
   const int eb = P->dtype == BS_F64 ? 8 : 2;
@@ -524,7 +529,7 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
     S.useful_bytes = (double)(populated_elems(P->A) + populated_elems(P->B)) * eb_in + (double)populated_elems(P->C) * eb_out;
     if (dtype == BS_F64) {
       S.tile_tasks = (int64_t)P->ts.tasks.size();
-      S.tail_tasks = (int64_t)(P->ts.tail_elems.size() / 2 + 31) / 32;   // warp-sized pieces of the tail list
+      S.tail_tasks = (int64_t)(P->ts.tail_elems.size() / 2 + kThreads - 1) / kThreads;   // CTA-sized pieces of the tail list
       S.tasks = S.tile_tasks + S.tail_tasks;
       S.executed_flops = P->ts.executed_flops;
     } else {
@@ -640,6 +645,10 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
     p.tail_elems = (const int2 *)P->d_tail;
     p.ntasks = (int32_t)P->ts.tasks.size();
     p.ntail = (int32_t)(P->ts.tail_elems.size() / 2);
+    p.nct = (int32_t)((p.ntail + kThreads - 1) / kThreads);
+    p.nq = (int32_t)P->ts.tq_ptr.size() - 1;
+    p.tq_ptr = P->d_tq_ptr;
+    p.tq_items = P->d_tq_items;
     p.counter = P->d_counter;
     p.status = P->d_status;
     BS_CUDA(launch_fp64_grouped(p, P->grid, s));
@@ -722,7 +731,7 @@ bs_status bs_plan_last_device_error(bs_plan *P, void *stream) {
   if (v != 0) {
     BS_CUDA(cudaMemset(P->d_status, 0, sizeof v));
     // a kernel that stopped early may leave the work counters set
-    BS_CUDA(cudaMemset(P->d_counter, 0, 16));
+    BS_CUDA(cudaMemset(P->d_counter, 0, P->counter_bytes));
   }
   if (v == DS_OK) return BS_OK;
   if (v == DS_TIMEOUT) return BS_ERR_TIMEOUT;

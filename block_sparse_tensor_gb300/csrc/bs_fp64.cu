@@ -4,8 +4,10 @@
 // The grouped kernel runs the whole task list of a plan in one launch
 // (uni20 design note "block coalescing", Summary: fewer, larger kernels;
 // the inferensys glossary "Sparse Operator Fusion": persistent thread blocks
-// and warp-level gather-compute-scatter).  Resident CTAs take tasks from a
-// global counter in longest-first order:
+// and warp-level gather-compute-scatter).  Resident CTAs first take tile tasks
+// from a global counter in longest-first order, then their warps take tail
+// warp-tasks from a queue per SM, dealt longest-first onto the least loaded
+// queue at plan time (and steal from other queues once their own is empty):
 //   - TILE: the CTA computes a tm x tn tile of one group.  Each K chunk of the
 //     group's concatenated inner axis is staged in shared memory through
 //     per-row and per-k address tables, so inner blocks of any size and any
@@ -55,6 +57,7 @@ struct TileSmem {
   int64_t kL[kKC];
   int64_t kB[kKC];
   int task;
+  int q0, qk;   // tail: this SM's queue and how many queues were emptied
 };
 
 __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
@@ -125,7 +128,7 @@ __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
 // One output per lane for 32 consecutive outputs of the tail list.  The loop
 // count is the warp's longest K; a lane whose group is shorter stops adding.
 // When every lane's group is one view (the usual case with panel layouts) the
-// loop is unrolled with two accumulators; otherwise each lane walks its
+// loop is unrolled with eight accumulators; otherwise each lane walks its
 // group's views, switching view on its own.
 __device__ void run_tail_warp(const Fp64Params &p, int w) {
   const int lane = threadIdx.x & 31;
@@ -147,14 +150,28 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
   int64_t ldb = k.ldb;
   double acc = 0.0;
   if (__all_sync(0xFFFFFFFFu, G.kseg_count == 1)) {
-    double acc1 = 0.0;
+    // eight independent chains with their loads issued ahead, so that a warp
+    // left alone on its SM at the end of the launch still keeps enough B rows
+    // in flight to feed the FP64 pipe; steps past this lane's K load nothing
+    // and add 0 * 0
+    constexpr int U = 8;
+    double a[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) a[u] = 0.0;
     int it = 0;
-    for (; it + 2 <= kmax; it += 2) {
-      if (it < kg) acc = fma(__ldg(ap + it), __ldg(bp + it * ldb), acc);
-      if (it + 1 < kg) acc1 = fma(__ldg(ap + it + 1), __ldg(bp + (it + 1) * ldb), acc1);
+    for (; it + U <= kmax; it += U) {
+      double x[U], y[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        x[u] = it + u < kg ? __ldg(ap + it + u) : 0.0;
+        y[u] = it + u < kg ? __ldg(bp + (it + u) * ldb) : 0.0;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) a[u] = fma(x[u], y[u], a[u]);
     }
-    if (it < kg) acc = fma(__ldg(ap + it), __ldg(bp + it * ldb), acc);
-    acc += acc1;
+    for (; it < kmax; ++it)
+      if (it < kg) a[0] = fma(__ldg(ap + it), __ldg(bp + it * ldb), a[0]);
+    acc = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
   } else {
     int si = 0, rem = k.klen;
     for (int it = 0; it < kmax; ++it) {
@@ -191,14 +208,45 @@ __global__ void __launch_bounds__(kThreads, 4) fp64_grouped_kernel(Fp64Params p)
     if (t >= p.ntasks) break;
     run_tile(p, p.tasks[t], sm);
   }
-  // then the tail list, 32 outputs per warp at a time
-  const int ntw = (p.ntail + 31) / 32;
-  for (;;) {
-    int w = 0;
-    if ((threadIdx.x & 31) == 0) w = (int)atomicAdd(&p.counter[2], 1u);
-    w = __shfl_sync(0xFFFFFFFFu, w, 0);
-    if (w >= ntw) break;
-    run_tail_warp(p, w);
+  // then the tail tasks: first the queue dealt to this SM, then, once it is
+  // empty, whatever is left in the others (so no output depends on every SM
+  // receiving CTAs).  Thread 0 finds the next task; the CTA runs it, warp w on
+  // the task's w-th 32 outputs.
+  if (p.nct > 0) {
+    if (threadIdx.x == 0) {
+      unsigned smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      sm.q0 = (int)(smid % (unsigned)p.nq);
+      sm.qk = 0;
+    }
+    const int warp = threadIdx.x >> 5;
+    for (;;) {
+      if (threadIdx.x == 0) {
+        int got = -1;
+        while (sm.qk < p.nq) {
+          if (sm.qk > 0 && *(volatile uint32_t *)&p.counter[2] >= (uint32_t)p.nct) {   // all taken
+            sm.qk = p.nq;
+            break;
+          }
+          const int q = sm.q0 + sm.qk < p.nq ? sm.q0 + sm.qk : sm.q0 + sm.qk - p.nq;
+          const int beg = p.tq_ptr[q], n = p.tq_ptr[q + 1] - beg;
+          const int i = (int)atomicAdd(&p.counter[kQueueCounterBase + q], 1u);
+          if (i < n) {
+            atomicAdd(&p.counter[2], 1u);
+            got = p.tq_items[beg + i];
+            break;
+          }
+          ++sm.qk;
+        }
+        sm.task = got;
+      }
+      __syncthreads();
+      const int ct = sm.task;
+      __syncthreads();
+      if (ct < 0) break;
+      const int w = ct * (kThreads / 32) + warp;
+      if (w * 32 < p.ntail) run_tail_warp(p, w);
+    }
   }
   __syncthreads();
   // The last CTA to leave returns the counters to zero for the next launch.
@@ -209,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 4) fp64_grouped_kernel(Fp64Params p)
     if (prev == gridDim.x - 1) {
       atomicExch(&p.counter[0], 0u);
       atomicExch(&p.counter[2], 0u);
+      for (int q = 0; q < p.nq; ++q) atomicExch(&p.counter[kQueueCounterBase + q], 0u);
       atomicExch(&p.counter[1], 0u);
     }
   }

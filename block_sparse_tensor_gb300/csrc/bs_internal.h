@@ -58,11 +58,12 @@ struct Group {
 enum TaskKind : int32_t { TK_TILE = 0 };
 
 // TK_TILE: one CTA computes rows m0 .. m0+tm-1, columns n0 .. n0+tn-1 of group `g`.
-// Small groups are not tasks: their outputs form the tail list
-// tail_elems[e] = {group, r << 16 | c}, groups in decreasing K, and each warp
-// takes 32 consecutive outputs at a time (one per lane) once the tile tasks
-// are all taken, so the lanes of one warp run loops of nearly equal length
-// and every FMA instruction carries (almost) 32 useful lanes.
+// Small groups are not tile tasks: their outputs form the tail list
+// tail_elems[e] = {group, r << 16 | c}, groups in decreasing K, row-major
+// inside a group.  A tail task is kThreads consecutive outputs, one per
+// thread, so the lanes of one warp run loops of nearly equal length (every
+// FMA instruction carries almost 32 useful lanes) and the warps of one CTA
+// walk the same B rows together.
 struct Task {
   int32_t kind;
   int32_t g;       // group
@@ -97,6 +98,11 @@ struct ZeroBlock {
   int32_t cols;
 };
 
+// Work counters of the FP64 kernel: three scalars, the status word at byte 128,
+// one counter per tail queue from byte 256.
+inline size_t counter_bytes(int nq) { return (size_t)(256 + 4 * nq + 255) / 256 * 256; }
+constexpr int kQueueCounterBase = 64;   // in uint32 units
+
 // Device status word values (first int of the status buffer).
 enum DeviceStatus : int32_t { DS_OK = 0, DS_TIMEOUT = 1, DS_BOUNDS = 2 };
 
@@ -109,9 +115,14 @@ struct Fp64Params {
   const RowSeg *rsegs;
   const KSeg *ksegs;
   const int2 *tail_elems;
+  const int32_t *tq_ptr;    // per-SM queues of tail tasks: queue q holds tq_items[tq_ptr[q] .. tq_ptr[q+1])
+  const int32_t *tq_items;  // tail task t covers tail_elems[kThreads t .. kThreads t + kThreads - 1]
   int32_t ntasks;
   int32_t ntail;       // outputs in the tail list
-  uint32_t *counter;   // [0] next tile task, [1] CTAs finished, [2] next tail warp; all return to 0
+  int32_t nct;         // tail tasks
+  int32_t nq;          // queues (one per SM of the planned device)
+  uint32_t *counter;   // [0] next tile task, [1] CTAs finished, [2] tail tasks taken;
+                       // counter[64 + q]: next item of queue q.  All return to 0 at exit.
   int32_t *status;
 };
 

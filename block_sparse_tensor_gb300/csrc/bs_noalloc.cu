@@ -71,11 +71,15 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   const size_t n_rsegs = P->gs.rsegs.size() * sizeof(RowSeg);
   const size_t n_ksegs = P->gs.ksegs.size() * sizeof(KSeg);
   const size_t n_tail = P->ts.tail_elems.size() * sizeof(int32_t);
+  const size_t n_tqp = P->ts.tq_ptr.size() * sizeof(int32_t);
+  const size_t n_tqi = P->ts.tq_items.size() * sizeof(int32_t);
+  const int nq = (int)std::max<size_t>(1, P->ts.tq_ptr.size()) - 1;
+  const size_t n_ctr = counter_bytes(nq);
   const size_t n_pack = P->pack_copies.size() * sizeof(PackCopy);
   const size_t n_zero = P->zero_blocks.size() * sizeof(ZeroBlock);
   const size_t n_ws_a = P->pack_a ? (size_t)P->A_pk.nelems * sizeof(double) : 0;
   const size_t n_ws_b = P->pack_b ? (size_t)P->B_pk.nelems * sizeof(double) : 0;
-  size_t off = 256;
+  size_t off = n_ctr;
   const size_t o_tasks = off;
   off = align256(off + n_tasks);
   const size_t o_groups = off;
@@ -86,6 +90,10 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   off = align256(off + n_ksegs);
   const size_t o_tail = off;
   off = align256(off + n_tail);
+  const size_t o_tqp = off;
+  off = align256(off + n_tqp);
+  const size_t o_tqi = off;
+  off = align256(off + n_tqi);
   const size_t o_pack = off;
   off = align256(off + n_pack);
   const size_t o_zero = off;
@@ -109,10 +117,11 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
     return n == 0 || cudaMemcpyAsync(b + o, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
   };
   // work counters and status word must start at zero; the rest is overwritten
-  if (cudaMemsetAsync(b, 0, 256, s) != cudaSuccess) return BS_ERR_CUDA;
+  if (cudaMemsetAsync(b, 0, n_ctr, s) != cudaSuccess) return BS_ERR_CUDA;
   if (!up(o_tasks, P->ts.tasks.data(), n_tasks) || !up(o_groups, P->gs.groups.data(), n_groups) ||
       !up(o_rsegs, P->gs.rsegs.data(), n_rsegs) || !up(o_ksegs, P->gs.ksegs.data(), n_ksegs) ||
-      !up(o_tail, P->ts.tail_elems.data(), n_tail) || !up(o_pack, P->pack_copies.data(), n_pack) ||
+      !up(o_tail, P->ts.tail_elems.data(), n_tail) || !up(o_tqp, P->ts.tq_ptr.data(), n_tqp) ||
+      !up(o_tqi, P->ts.tq_items.data(), n_tqi) || !up(o_pack, P->pack_copies.data(), n_pack) ||
       !up(o_zero, P->zero_blocks.data(), n_zero))
     return BS_ERR_CUDA;
 
@@ -146,6 +155,10 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   p.tail_elems = (const int2 *)(b + o_tail);
   p.ntasks = (int32_t)P->ts.tasks.size();
   p.ntail = (int32_t)ntail;
+  p.nct = (int32_t)((ntail + kThreads - 1) / kThreads);
+  p.nq = nq;
+  p.tq_ptr = (const int32_t *)(b + o_tqp);
+  p.tq_items = (const int32_t *)(b + o_tqi);
   p.counter = (uint32_t *)b;
   p.status = (int32_t *)(b + 128);
   const int64_t items = (int64_t)P->ts.tasks.size() + (ntail + kThreads - 1) / kThreads;

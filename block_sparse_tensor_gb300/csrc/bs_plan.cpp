@@ -306,6 +306,8 @@ static inline int64_t lanes(int64_t e) { return (e + 31) / 32 * 32; }
 void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
   ts->tasks.clear();
   ts->tail_elems.clear();
+  ts->tq_ptr.clear();
+  ts->tq_items.clear();
   std::vector<std::pair<double, Task>> costed;
   std::vector<int32_t> tails;
   double exec = 0, work = 0;
@@ -350,7 +352,37 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
         elem_k.push_back(G.k);
       }
   }
-  for (size_t w = 0; w < elem_k.size(); w += 32) exec += 2.0 * 32.0 * elem_k[w];   // lane 0 holds the warp's longest K
+  // Tail tasks of kThreads outputs (one CTA, one output per thread): the 8
+  // warps of a task hold consecutive outputs of the same group(s), so they
+  // walk the same B rows together and share them through L1.  Tasks are dealt
+  // to one queue per SM, longest first onto the least loaded queue, so every
+  // SM starts with the same amount of FP64 work whatever order its CTAs
+  // arrive in.  Lane 0 of each warp holds that warp's longest K.
+  const int nct = (int)((elem_k.size() + kThreads - 1) / kThreads);
+  // no more queues than a few tasks each can fill (SMs then share a queue)
+  const int nq = std::max(1, std::min(pm.sms, nct / 4));
+  std::vector<std::vector<int32_t>> queues(nq);
+  std::vector<std::pair<double, int>> heap;   // (load, queue) min-heap
+  for (int q = 0; q < nq; ++q) heap.push_back({0.0, q});
+  auto cmp = [](const std::pair<double, int> &a, const std::pair<double, int> &b) { return a.first > b.first; };
+  std::make_heap(heap.begin(), heap.end(), cmp);
+  for (int ct = 0; ct < nct; ++ct) {
+    double cost = 64.0;   // fixed cost per task
+    for (size_t w = (size_t)ct * kThreads; w < std::min(elem_k.size(), (size_t)(ct + 1) * kThreads); w += 32) {
+      exec += 2.0 * 32.0 * elem_k[w];
+      cost += elem_k[w];
+    }
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    heap.back().first += cost;
+    queues[heap.back().second].push_back(ct);
+    std::push_heap(heap.begin(), heap.end(), cmp);
+  }
+  ts->tq_ptr.assign(nq + 1, 0);
+  ts->tq_items.clear();
+  for (int q = 0; q < nq; ++q) {
+    ts->tq_items.insert(ts->tq_items.end(), queues[q].begin(), queues[q].end());
+    ts->tq_ptr[q + 1] = (int32_t)ts->tq_items.size();
+  }
   // longest processing time first for the dynamic scheduler
   std::stable_sort(costed.begin(), costed.end(),
                    [](const std::pair<double, Task> &a, const std::pair<double, Task> &b) { return a.first > b.first; });
