@@ -48,6 +48,22 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank number over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(per_rank_units: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank processes the same units; time is the slowest rank's."""
+    return world * per_rank_units / (ms_max * 1e-3)
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -222,13 +238,9 @@ def run_gpu(args):
         torch.distributed.barrier()
     clocks = sampler.stop()
     assert bs.last_device_error(pb.P, stream) == 0
-    ms = statistics.mean(times)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * st["useful_flops"] / (ms * 1e-3) / 1e9
-    blocks_s = world * st["triples"] / (ms * 1e-3)
+    ms = max_over_ranks(statistics.mean(times), device="cuda")
+    value = weak_scaling_value(st["useful_flops"], world, ms) / 1e9
+    blocks_s = weak_scaling_value(st["triples"], world, ms)
 
     # end to end through the host-buffer entry point, pinned buffers
     a_pin = torch.from_numpy(pb.a_host).pin_memory()
