@@ -132,21 +132,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-bs_status encode_maps(bs_plan *P, const void *A, const void *B, const void *C) {
+bs_status encode_maps(bs_plan *P, const void *A, const void *B) {
   auto enc = get_encode();
   if (!enc) return BS_ERR_CUDA;
   P->map_bytes.assign(P->maps.size() * sizeof(CUtensorMap), 0);
   for (size_t t = 0; t < P->maps.size(); ++t) {
     const MapDesc &m = P->maps[t];
-    const int eb = m.operand == 2 ? 4 : 2;
-    const char *base = (const char *)(m.operand == 0 ? A : m.operand == 1 ? B : C) + m.off * eb;
+    const int eb = 2;
+    const char *base = (const char *)(m.operand == 0 ? A : B) + m.off * eb;
     cuuint64_t dims[2] = {(cuuint64_t)m.inner, (cuuint64_t)m.outer};
     cuuint64_t strides[1] = {(cuuint64_t)(m.ld * eb)};
     cuuint32_t box[2] = {(cuuint32_t)m.box_inner, (cuuint32_t)m.box_outer};
     cuuint32_t es[2] = {1, 1};
     CUtensorMap *out = (CUtensorMap *)(P->map_bytes.data() + t * sizeof(CUtensorMap));
-    CUresult r = enc(out, m.operand == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                     (void *)base, dims, strides, box, es,
+    CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)base, dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return BS_ERR_MISALIGNED;
@@ -176,12 +175,13 @@ void build_bf16(bs_plan *P) {
     for (int32_t s = 0; s < g.kseg_count; ++s) {
       const KSeg &k = gs.ksegs[g.kseg_begin + s];
       Bf16Pair pr{};
-      pr.map_a = map_id(0, k.ka, k.klen, g.m, k.kl, 64, 128);
+      pr.map_a = map_id(0, k.ka, k.klen, g.m, k.kl, 64, 128 * kBf16MaxHalves);
       pr.map_b = map_id(1, k.kb, g.n, k.klen, k.ldb, 64, 64);
       pr.klen = k.klen;
       P->bpairs.push_back(pr);
     }
-    for (int32_t m0 = 0; m0 < g.m; m0 += 128)
+    // tiles of kBf16MaxHalves x 128 rows; two halves share each B tile
+    for (int32_t m0 = 0; m0 < g.m; m0 += 128 * kBf16MaxHalves)
       for (int32_t n0 = 0; n0 < g.n; n0 += 256) {
         Bf16Task t{};
         t.pair_begin = pb;
@@ -191,13 +191,13 @@ void build_bf16(bs_plan *P) {
         t.m = g.m;
         t.n = g.n;
         t.bn = (std::min(256, g.n - n0) + 15) / 16 * 16;
+        t.mh = (int16_t)(kBf16MaxHalves == 2 && g.m - m0 > 128 ? 2 : 1);
         t.c_off = rs.rc;
         t.ldc = rs.ldc;
-        // C is written by TMA stores when its view obeys the 16-byte rules
-        t.map_c = tma_ok(rs.rc, rs.ldc, 4) ? map_id(2, rs.rc, g.n, g.m, rs.ldc, 32, 32) : -1;
+        t.c_vec = (int16_t)(tma_ok(rs.rc, rs.ldc, 4) ? 1 : 0);   // 16-byte aligned rows: vector stores
         int64_t kch = 0;
         for (int32_t s = 0; s < g.kseg_count; ++s) kch += (gs.ksegs[g.kseg_begin + s].klen + 63) / 64;
-        costed.push_back({(double)kch * (t.bn + 64), t});
+        costed.push_back({(double)kch * (t.bn * t.mh + 64), t});
       }
   }
   std::stable_sort(costed.begin(), costed.end(),
@@ -538,7 +538,7 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
       for (const auto &t : P->btasks) {
         int64_t kk = 0;
         for (int32_t s = 0; s < t.pair_count; ++s) kk += (P->bpairs[t.pair_begin + s].klen + 15) / 16 * 16;
-        ex += 2.0 * 128 * t.bn * kk;
+        ex += 2.0 * 128 * t.mh * t.bn * kk;
       }
       S.executed_flops = ex;
     }
@@ -655,14 +655,13 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
   } else {
     if (((uintptr_t)Ause | (uintptr_t)Buse | (uintptr_t)C) % 16 != 0) return BS_ERR_MISALIGNED;
     if (P->btasks.empty()) return BS_OK;
-    if (P->maps_a_ptr != Ause || P->maps_b_ptr != Buse || P->maps_c_ptr != C) {
-      bs_status st = encode_maps(P, Ause, Buse, C);
+    if (P->maps_a_ptr != Ause || P->maps_b_ptr != Buse) {
+      bs_status st = encode_maps(P, Ause, Buse);
       if (st != BS_OK) return st;
       BS_CUDA(cudaMemcpyAsync(P->d_maps, P->map_bytes.data(), P->map_bytes.size(), cudaMemcpyHostToDevice, s));
       BS_CUDA(cudaStreamSynchronize(s));
       P->maps_a_ptr = Ause;
       P->maps_b_ptr = Buse;
-      P->maps_c_ptr = C;
     }
     Bf16Params p{};
     p.maps = P->d_maps;

@@ -4,19 +4,26 @@
 // The tensor-core path is taken only where a coalesced group is a genuine
 // dense contraction in a type with a tensor-core path (uni20 design note
 // "block coalescing", "Two coalescing modes": a single-axis group is one
-// zero-waste GEMM).  One task is a 128 x BN tile (BN <= 256) of one
-// contraction-axis group; its K loop walks the group's inner segments, each
-// with its own tensor maps for the A view (group rows x d_k) and the B view
-// (d_k x group columns).  The copy engine fills everything past a view's edge
-// with zeros, so ragged d_k needs no padding in memory and adds nothing.
+// zero-waste GEMM).  One task is a (128 * mh) x BN tile (BN <= 256, mh = 1 by
+// default; mh = 2 puts two 128-row halves in two TMEM accumulators that share
+// every B tile) of one contraction-axis group.  The K loop walks the group's
+// inner segments, each with its own tensor maps for the A view (group rows x
+// d_k) and the B view (d_k x group columns).  The copy engine fills
+// everything past a view's edge with zeros, so ragged d_k needs no padding in
+// memory and adds nothing.
 //
-// Warp roles (192 threads, one CTA per SM, tasks striped over CTAs):
-//   warp 0  TMA producer: A tile 128 x 64 (K-major, 128-byte swizzle) and B
-//           tile 64 x BN (N-major, 128-byte swizzle) per stage, 4 stages;
-//   warp 1  TMEM owner and MMA issuer (one thread): 4 x (M128, N=BN, K16) per
-//           stage into one of two 256-column FP32 accumulators;
-//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, staged through
-//           swizzled shared memory, TMA tensor stores clipped at the group edge.
+// Warp roles (320 threads, one CTA per SM, tasks striped over CTAs in
+// longest-first order; each CTA's first task descriptors are preloaded to
+// shared memory in one round trip):
+//   warp 0  TMA producer: A box (128 * kBf16MaxHalves) x 64 (K-major,
+//           128-byte swizzle) and B boxes 64 x 64 (N-major, 128-byte swizzle);
+//   warp 1  TMEM owner and MMA issuer (one thread): per 16-wide K step one
+//           M128 x N=BN x K16 MMA per half, into 256-column FP32 slots used in
+//           rotation, so the epilogue of one tile overlaps the next tile;
+//   warps 2-9  epilogue, two warps per 32-lane TMEM quarter: tcgen05.ld of 32
+//           columns at a time, a swizzled shared-memory transpose, coalesced
+//           masked stores (plain stores: the copy engine serves only loads,
+//           and no padding byte of C is written).
 // Every wait is bounded by the global timer; on expiry the kernel records
 // a timeout in the status word, drains its copies and MMAs (again bounded),
 // frees its tensor memory and returns.
@@ -28,15 +35,19 @@ namespace bs {
 
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kBM = 128;
-constexpr int kBK = 64;
-constexpr int kATileBytes = kBM * kBK * 2;        // 16 KB
-constexpr int kBChunkBytes = 64 * kBK * 2;        // one 64-column N chunk: 8 KB
+constexpr int kStages = kBf16MaxHalves == 2 ? 3 : 4;
+constexpr int kBM = 128;                          // rows of one accumulator (UMMA M)
+constexpr int kBK = 64;                           // K per stage (one 128-byte swizzle row of BF16)
+constexpr int kAHalfBytes = kBM * kBK * 2;        // 16 KB: 128 rows of A
+constexpr int kATileBytes = kBf16MaxHalves * kAHalfBytes;   // one A box of 128 or 256 rows
+constexpr int kBChunkBytes = 64 * kBK * 2;        // one 64-column N chunk of B: 8 KB
 constexpr int kBTileBytes = 4 * kBChunkBytes;     // BN up to 256
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
-constexpr int kTmemCols = 512;
-constexpr int kThreadsBf16 = 192;
+constexpr int kTmemCols = 512;                    // two 256-column FP32 accumulator slots
+constexpr int kEpiWarps = 8;                      // two epilogue warps per TMEM lane quarter
+constexpr int kThreadsBf16 = 64 + 32 * kEpiWarps;
+constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x 32 FP32 columns per epilogue warp
+constexpr int kTaskCache = 16;                    // this CTA's first tasks, preloaded to shared memory
 
 struct Ctl {
   uint64_t full[kStages];
@@ -49,10 +60,10 @@ struct Ctl {
 };
 
 constexpr int kCtlBytes = 256;                    // Ctl rounded up
-constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x 32 FP32 columns
-constexpr size_t kSmemBytes =
-    1024 /*align slack*/ + (size_t)kStages * kStageBytes + kCtlBytes + 4 * 2 * kEpiBufBytes;
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kEpiBufBytes +
+                              kCtlBytes + kTaskCache * sizeof(Bf16Task);
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -102,16 +113,13 @@ __device__ __forceinline__ void prefetch_map(const void *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
-// Warm the descriptor cache with every tensor map task `t` will use.
-__device__ __forceinline__ void prefetch_task_maps(const Bf16Params &p, const char *maps, int t) {
-  if (t >= p.ntasks) return;
-  const Bf16Task T = p.tasks[t];
+// Warm the descriptor cache with every tensor map a task will use.
+__device__ __forceinline__ void prefetch_task_maps(const Bf16Params &p, const char *maps, const Bf16Task &T) {
   for (int q = 0; q < T.pair_count; ++q) {
     const Bf16Pair pr = p.pairs[T.pair_begin + q];
     prefetch_map(maps + (size_t)pr.map_a * 128);
     prefetch_map(maps + (size_t)pr.map_b * 128);
   }
-  if (T.map_c >= 0) prefetch_map(maps + (size_t)T.map_c * 128);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint32_t mbar, int x, int y) {
@@ -149,16 +157,20 @@ __device__ __forceinline__ void mma_commit(uint32_t mbar) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
-  uint32_t r[16];
+// 32 consecutive FP32 columns of this thread's TMEM lane, one wait for all.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+  uint32_t r[32];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void record_timeout(const Bf16Params &p, Ctl *ctl) {
@@ -166,13 +178,20 @@ __device__ __forceinline__ void record_timeout(const Bf16Params &p, Ctl *ctl) {
   atomicExch(p.status, (int32_t)DS_TIMEOUT);
 }
 
+__device__ __forceinline__ Bf16Task task_at(const Bf16Params &p, const Bf16Task *cache, int ti, int t) {
+  return ti < kTaskCache ? cache[ti] : p.tasks[t];
+}
+
 __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf16Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // [stages | epilogue staging, 1024-aligned for the 128-byte swizzle | control block]
-  Ctl *ctl = (Ctl *)(smem + (size_t)kStages * kStageBytes + 4 * 2 * kEpiBufBytes);
+  // [stages | epilogue staging, 1024-aligned for the 128-byte swizzle | control block | task cache]
+  unsigned char *epi_base = smem + (size_t)kStages * kStageBytes;
+  Ctl *ctl = (Ctl *)(epi_base + (size_t)kEpiWarps * kEpiBufBytes);
+  Bf16Task *cache = (Bf16Task *)((unsigned char *)ctl + kCtlBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int32_t *abort_flag = &ctl->abort_flag;
+  const char *maps = (const char *)p.maps;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -181,7 +200,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
-      mbar_init(smem_u32(&ctl->tempty[a]), 4);
+      mbar_init(smem_u32(&ctl->tempty[a]), kEpiWarps);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
@@ -194,6 +213,11 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // the epilogue warps preload this CTA's first task descriptors in one round trip
+  for (int i = threadIdx.x - 64; i >= 0 && i < kTaskCache; i += kThreadsBf16 - 64) {
+    const int t = blockIdx.x + i * gridDim.x;
+    if (t < p.ntasks) cache[i] = p.tasks[t];
+  }
   fence_before();
   __syncthreads();
   fence_after();
@@ -202,17 +226,16 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      const char *maps = (const char *)p.maps;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      uint32_t issued_phase[kStages];
-      bool outstanding[kStages];
-      for (int s = 0; s < kStages; ++s) outstanding[s] = false;
-      prefetch_task_maps(p, maps, blockIdx.x);
-      for (int t = blockIdx.x; ok && t < p.ntasks; t += gridDim.x) {
-        const Bf16Task T = p.tasks[t];
-        prefetch_task_maps(p, maps, t + gridDim.x);   // the next task's descriptors load while this one streams
+      uint32_t outstanding = 0, issued_phase = 0;   // bit s: stage s has a copy in flight / its phase
+      if (blockIdx.x < p.ntasks) prefetch_task_maps(p, maps, cache[0]);
+      int ti = 0;
+      for (int t = blockIdx.x; ok && t < p.ntasks; t += gridDim.x, ++ti) {
+        const Bf16Task T = task_at(p, cache, ti, t);
+        if (t + (int)gridDim.x < p.ntasks)   // the next task's descriptors load while this one streams
+          prefetch_task_maps(p, maps, task_at(p, cache, ti + 1, t + gridDim.x));
         const int nb = (T.bn + 63) / 64;
         const uint32_t bytes = kATileBytes + nb * kBChunkBytes;
         for (int q = 0; ok && q < T.pair_count; ++q) {
@@ -226,7 +249,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
               break;
             }
             const uint32_t fb = smem_u32(&ctl->full[stage]);
-            if ((p.debug_flags & 1) && blockIdx.x == 0 && t == (int)blockIdx.x && q == 0 && kc == 0) {
+            if ((p.debug_flags & 1) && blockIdx.x == 0 && ti == 0 && q == 0 && kc == 0) {
               // test hook: this stage is never filled, so the MMA thread's
               // bounded wait on it runs out and the kernel reports a timeout
               if (++stage == kStages) {
@@ -237,11 +260,11 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
             }
             mbar_expect_tx(fb, bytes);
             unsigned char *st = smem + (size_t)stage * kStageBytes;
-            tma_load_2d(smem_u32(st), ma, fb, kc, T.m0);
+            tma_load_2d(smem_u32(st), ma, fb, kc, T.m0);   // rows past the group read as zero
             for (int c = 0; c < nb; ++c)
               tma_load_2d(smem_u32(st + kATileBytes + c * kBChunkBytes), mb, fb, T.n0 + 64 * c, kc);
-            outstanding[stage] = true;
-            issued_phase[stage] = phase;
+            outstanding |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -252,30 +275,48 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       // Drain: every issued stage completes its transfer before the CTA exits.
       // (On the normal path the MMA thread has consumed them all already.)
       for (int s = 0; s < kStages; ++s)
-        if (outstanding[s]) {
+        if (outstanding >> s & 1u) {
           uint64_t t0 = gtime();
-          while (!mbar_try(smem_u32(&ctl->full[s]), issued_phase[s]) && gtime() - t0 < p.timeout_ns) {
+          while (!mbar_try(smem_u32(&ctl->full[s]), issued_phase >> s & 1u) && gtime() - t0 < p.timeout_ns) {
           }
         }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
+      // Accumulator slots: a two-half task uses both, a one-half task the next
+      // one in rotation; the epilogue walks the same sequence.  Everything the
+      // issue loop touches stays in scalar registers (a local array here cost
+      // more than half the tensor throughput).
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      int rot = 0;
+      uint32_t te0 = 0, te1 = 0;   // tempty phase per slot
       bool ok = true;
       bool issued_any = false;
-      for (int t = blockIdx.x; ok && t < p.ntasks; t += gridDim.x) {
-        const Bf16Task T = p.tasks[t];
+      int ti = 0;
+      for (int t = blockIdx.x; ok && t < p.ntasks; t += gridDim.x, ++ti) {
+        const Bf16Task T = task_at(p, cache, ti, t);
         const uint32_t idesc = instr_desc(T.bn);
-        if (!mbar_wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+        const bool two = T.mh == 2;
+        const int s0 = two ? 0 : rot;
+        if (!two) rot ^= 1;
+        if (!mbar_wait(smem_u32(&ctl->tempty[s0]), (s0 ? te1 : te0) ^ 1u, abort_flag, p.timeout_ns)) {
           record_timeout(p, ctl);
           break;
         }
+        if (s0) te1 ^= 1u;
+        else te0 ^= 1u;
+        if (two) {
+          if (!mbar_wait(smem_u32(&ctl->tempty[1]), te1 ^ 1u, abort_flag, p.timeout_ns)) {
+            record_timeout(p, ctl);
+            break;
+          }
+          te1 ^= 1u;
+        }
         fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+        const uint32_t d0 = tmem_base + (uint32_t)(s0 * 256);
+        const uint32_t d1 = tmem_base + 256u;
         uint32_t accumulate = 0;
         for (int q = 0; ok && q < T.pair_count; ++q) {
           const int klen = p.pairs[T.pair_begin + q].klen;
@@ -290,9 +331,9 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
             const uint32_t b0 = a0 + kATileBytes;
             const int ksteps = min(4, (klen - kc + 15) / 16);
             for (int ks = 0; ks < ksteps; ++ks) {
-              const uint64_t ad = smem_desc(a0 + ks * 32, 16, 1024);
               const uint64_t bd = smem_desc(b0 + ks * 2048, kBChunkBytes, 1024);
-              mma_bf16(d_tmem, ad, bd, idesc, accumulate);
+              mma_bf16(d0, smem_desc(a0 + ks * 32, 16, 1024), bd, idesc, accumulate);
+              if (two) mma_bf16(d1, smem_desc(a0 + kAHalfBytes + ks * 32, 16, 1024), bd, idesc, accumulate);
               accumulate = 1;
             }
             mma_commit(smem_u32(&ctl->empty[stage]));
@@ -304,11 +345,8 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
           }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&ctl->tfull[acc]));
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
+        mma_commit(smem_u32(&ctl->tfull[s0]));
+        if (two) mma_commit(smem_u32(&ctl->tfull[1]));
       }
       // Drain: all MMAs issued by this thread finish before tensor memory is freed.
       if (issued_any) {
@@ -320,74 +358,80 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    // Each warp owns TMEM lanes 32*quarter .. +31 (tile rows) and two 4 KB
-    // staging buffers.  A 32 x 32 FP32 chunk goes TMEM -> registers -> shared
-    // memory (128-byte swizzle, so the 32 row writes of one column group hit
-    // distinct banks) -> one TMA tensor store, which clips rows and columns
-    // past the group's edge.  Unaligned C views fall back to direct stores.
+    // A warp may read only TMEM lanes 32*(warp%4) .. +31 (tile rows).  Each
+    // 32 x 32 FP32 chunk goes TMEM -> registers -> shared memory (row per
+    // lane, 16-byte pieces XOR-swizzled by row so both the row writes and
+    // the column reads are free of bank conflicts) -> coalesced global stores
+    // of four 128-byte row segments per instruction, masked at the group edge.
     const int quarter = warp & 3;
-    unsigned char *stage_buf = smem + (size_t)kStages * kStageBytes + (size_t)quarter * 2 * kEpiBufBytes;
-    const char *maps = (const char *)p.maps;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    int buf = 0;
-    for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
-      const Bf16Task T = p.tasks[t];
-      if (!mbar_wait(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, p.timeout_ns)) {
+    const int ew = warp - 2;
+    const int grp = ew >> 2;                  // 0 or 1: which half (two-half tasks) or which chunks
+    unsigned char *stg = epi_base + (size_t)ew * kEpiBufBytes;
+    int rot = 0;
+    uint32_t tf0 = 0, tf1 = 0;   // tfull phase per slot
+    int ti = 0;
+    for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x, ++ti) {
+      const Bf16Task T = task_at(p, cache, ti, t);
+      const bool two = T.mh == 2;
+      const int s0 = two ? 0 : rot;
+      if (!two) rot ^= 1;
+      if (!mbar_wait(smem_u32(&ctl->tfull[s0]), s0 ? tf1 : tf0, abort_flag, p.timeout_ns)) {
         if (lane == 0) record_timeout(p, ctl);
         break;
       }
+      if (s0) tf1 ^= 1u;
+      else tf0 ^= 1u;
+      if (two) {
+        if (!mbar_wait(smem_u32(&ctl->tfull[1]), tf1, abort_flag, p.timeout_ns)) {
+          if (lane == 0) record_timeout(p, ctl);
+          break;
+        }
+        tf1 ^= 1u;
+      }
       fence_after();
-      const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * 256);
-      if (T.map_c >= 0 && T.m0 + quarter * 32 < T.m) {   // quarters wholly past the last row store nothing
-        const void *mc = maps + (size_t)T.map_c * 128;
-        for (int c0 = 0; c0 < T.bn; c0 += 32) {
+      const int my_slot = two ? grp : s0;
+      const int row0 = T.m0 + (two ? 128 * grp : 0) + 32 * quarter;
+      const int c_first = two ? 0 : 32 * grp, c_step = two ? 32 : 64;
+      if (row0 < T.m) {
+        const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(my_slot * 256);
+        float *cbase = p.C + T.c_off;
+        for (int c0 = c_first; c0 < T.bn; c0 += c_step) {
           float v[32];
-          tmem_ld16(trow + c0, v);
-          tmem_ld16(trow + c0 + 16, v + 16);
-          // the buffer written two chunks ago must have been read by its store
-          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-          __syncwarp();
-          unsigned char *b = stage_buf + buf * kEpiBufBytes + lane * 128;
+          tmem_ld32(trow + c0, v);
+          unsigned char *mine = stg + lane * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            *(float4 *)(b + ((j ^ (lane & 7)) << 4)) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            *(float4 *)(mine + ((j ^ (lane & 7)) << 4)) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           __syncwarp();
-          if (lane == 0) {
-            asm volatile(
-                "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(mc),
-                "r"(smem_u32(stage_buf + buf * kEpiBufBytes)), "r"(T.n0 + c0), "r"(T.m0 + quarter * 32)
-                : "memory");
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-          }
-          buf ^= 1;
-        }
-      } else if (T.map_c < 0) {
-        const int row = T.m0 + quarter * 32 + lane;
-        const bool row_ok = row < T.m;
-        float *crow = p.C + T.c_off + (int64_t)row * T.ldc + T.n0;
-        const int ncols = min(T.bn, T.n - T.n0);
-        for (int c0 = 0; c0 < T.bn; c0 += 16) {
-          float v[16];
-          tmem_ld16(trow + c0, v);
-          if (!row_ok) continue;
+          const int j = lane & 7;
+          const int gcol = T.n0 + c0 + 4 * j;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c0 + i < ncols) crow[c0 + i] = v[i];
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            const int grow = row0 + r;
+            const float4 x = *(const float4 *)(stg + r * 128 + ((j ^ (r & 7)) << 4));
+            if (grow < T.m) {
+              float *dst = cbase + (int64_t)grow * T.ldc + gcol;
+              if (T.c_vec && gcol + 4 <= T.n) {
+                *(float4 *)dst = x;
+              } else {
+                if (gcol + 0 < T.n) dst[0] = x.x;
+                if (gcol + 1 < T.n) dst[1] = x.y;
+                if (gcol + 2 < T.n) dst[2] = x.z;
+                if (gcol + 3 < T.n) dst[3] = x.w;
+              }
+            }
+          }
+          __syncwarp();
         }
       }
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&ctl->tempty[s0]));
+        if (two) mbar_arrive(smem_u32(&ctl->tempty[1]));
       }
     }
-    // staged stores finish reading shared memory before the CTA can exit
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    __syncwarp();
   }
   fence_before();
   __syncthreads();

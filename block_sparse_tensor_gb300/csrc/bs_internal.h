@@ -135,9 +135,12 @@ struct PackParams {
 };
 
 // ---- BF16 tensor-core path ------------------------------------------------
-// One task = a 128 x BN tile of a contraction-axis group; its K loop walks the
-// group's block pairs, each with its own tensor maps (zero fill past the
-// block edge keeps ragged K exact).
+// One task = a (128 * mh) x BN tile of a contraction-axis group (mh = 1 or 2
+// row halves, each with its own TMEM accumulator; both halves share every B
+// tile); its K loop walks the group's block pairs, each with its own tensor
+// maps (zero fill past the block edge keeps ragged K exact).
+constexpr int kBf16MaxHalves = 1;     // 128-row halves per BF16 tile (1: 128-row tiles, 2: 256-row tiles)
+
 struct Bf16Pair {
   int32_t map_a;   // index of the A tensor map (rows of the group x d_k)
   int32_t map_b;   // index of the B tensor map (d_k x cols of the group)
@@ -153,7 +156,8 @@ struct Bf16Task {
   int32_t m;         // rows of the group
   int32_t n;         // columns of the group
   int32_t bn;        // UMMA N of the tile (multiple of 16, <= 256)
-  int32_t map_c;     // tensor map of the group's C view, or -1 for direct stores
+  int16_t mh;        // 128-row halves in the tile: 1 or 2 (each its own TMEM accumulator)
+  int16_t c_vec;     // 1 when every C row of the group starts 16-byte aligned (vector stores)
   int64_t c_off;     // C offset of the group's (0, 0) element
   int64_t ldc;
 };

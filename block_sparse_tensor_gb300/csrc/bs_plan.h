@@ -49,7 +49,7 @@ double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm,
 // Host description of one TMA tensor map of the BF16 path (encoded per call
 // with the caller's base pointer, then cached while the pointers stay the same).
 struct MapDesc {
-  int32_t operand;      // 0: A, 1: B, 2: C (FP32)
+  int32_t operand;      // 0: A, 1: B
   int64_t off;          // element offset of the view's first element
   int64_t inner;        // contiguous extent (elements)
   int64_t outer;        // rows
@@ -77,7 +77,7 @@ struct bs_plan {
   std::vector<bs::Bf16Pair> bpairs;
   std::vector<bs::MapDesc> maps;
   std::vector<unsigned char> map_bytes;   // encoded maps (128 bytes each)
-  const void *maps_a_ptr = nullptr, *maps_b_ptr = nullptr, *maps_c_ptr = nullptr;
+  const void *maps_a_ptr = nullptr, *maps_b_ptr = nullptr;
   // device state
   int device = -1;
   int sm_count = 0;

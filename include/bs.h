@@ -215,11 +215,8 @@ bs_status bs_plan_triples(const bs_plan *plan, int64_t *ntriples, int64_t *ngrou
 
 /* Enqueue C = A B on `stream` and return at once.  A, B, C are device
  * pointers to buffers laid out per the plan's A, B and C layouts; every
- * populated C element is overwritten, absent blocks are not touched, and
- * padding is not touched, with one exception: BF16 plans write C through the
- * tensor-memory copy engine, which stores whole 16-byte granules, so the
- * alignment padding that completes the last 16-byte granule of a C block row
- * (ALIGN16 layouts only) is set to zero.  A, B and C must not overlap.  Work: an optional gather, an optional
+ * populated C element is overwritten; padding and absent blocks are not
+ * touched.  A, B and C must not overlap.  Work: an optional gather, an optional
  * zero fill of C, one persistent grouped-GEMM kernel.  BF16 plans need A and B
  * 16-byte aligned (MISALIGNED otherwise).  A plan holds one workspace and one
  * work counter: do not run the same plan on two streams at once.  Errors found
