@@ -203,6 +203,27 @@ void build_bf16(bs_plan *P) {
   std::stable_sort(costed.begin(), costed.end(),
                    [](const std::pair<double, Bf16Task> &a, const std::pair<double, Bf16Task> &b) { return a.first > b.first; });
   for (auto &c : costed) P->btasks.push_back(c.second);
+  // One CTA per SM; each task goes, longest first, to the CTA with the least
+  // modelled work.  A stage costs a fixed handoff plus MMA time growing with BN.
+  const int ncta = std::max(1, std::min<int>((int)P->btasks.size(), P->sm_count > 0 ? P->sm_count : 152));
+  std::vector<std::vector<int32_t>> lists(ncta);
+  std::vector<std::pair<double, int>> heap;
+  for (int c = 0; c < ncta; ++c) heap.push_back({0.0, c});
+  auto cmp = [](const std::pair<double, int> &a, const std::pair<double, int> &b) { return a.first > b.first; };
+  for (size_t t = 0; t < P->btasks.size(); ++t) {
+    const Bf16Task &T = P->btasks[t];
+    int64_t st = 0;
+    for (int32_t q = 0; q < T.pair_count; ++q) st += (P->bpairs[T.pair_begin + q].klen + 63) / 64;
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    heap.back().first += 150.0 + (double)st * (96.0 + T.bn * T.mh);
+    lists[heap.back().second].push_back((int32_t)t);
+    std::push_heap(heap.begin(), heap.end(), cmp);
+  }
+  P->bcta_ptr.assign(ncta + 1, 0);
+  for (int c = 0; c < ncta; ++c) {
+    P->bcta_items.insert(P->bcta_items.end(), lists[c].begin(), lists[c].end());
+    P->bcta_ptr[c + 1] = (int32_t)P->bcta_items.size();
+  }
 }
 
 bs_status upload(bs_plan *P) {
@@ -218,6 +239,8 @@ bs_status upload(bs_plan *P) {
   size_t o_zero = append_bytes(buf, P->zero_blocks);
   size_t o_bt = append_bytes(buf, P->btasks);
   size_t o_bp = append_bytes(buf, P->bpairs);
+  size_t o_bcp = append_bytes(buf, P->bcta_ptr);
+  size_t o_bci = append_bytes(buf, P->bcta_items);
   std::vector<unsigned char> mapspace(P->maps.size() * sizeof(CUtensorMap), 0);
   size_t o_maps = append_bytes(buf, mapspace);
   size_t total = (buf.size() + 255) / 256 * 256 + 256;
@@ -236,6 +259,8 @@ bs_status upload(bs_plan *P) {
   P->d_pack = (PackCopy *)(b + o_pack);
   P->d_zero = (ZeroBlock *)(b + o_zero);
   P->d_btasks = (Bf16Task *)(b + o_bt);
+  P->d_bcta_ptr = (int32_t *)(b + o_bcp);
+  P->d_bcta_items = (int32_t *)(b + o_bci);
   P->d_bpairs = (Bf16Pair *)(b + o_bp);
   P->d_maps = (void *)(b + o_maps);
   // counters and status word: zero once, kernels return them to zero
@@ -555,7 +580,7 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
         const int64_t work_items = (int64_t)P->ts.tasks.size() + (int64_t)(P->ts.tail_elems.size() / 2 + kThreads - 1) / kThreads;
         P->grid = (int)std::max<int64_t>(1, std::min<int64_t>(work_items, (int64_t)P->sm_count * cps));
       }
-      else P->grid = std::max(1, std::min<int>((int)P->btasks.size(), P->sm_count));
+      else P->grid = std::max(1, (int)P->bcta_ptr.size() - 1);
     }
   } catch (const std::bad_alloc &) {
     free_device(P);
@@ -666,6 +691,8 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
     Bf16Params p{};
     p.maps = P->d_maps;
     p.tasks = P->d_btasks;
+    p.cta_ptr = P->d_bcta_ptr;
+    p.cta_items = P->d_bcta_items;
     p.pairs = P->d_bpairs;
     p.C = (float *)C;
     p.ntasks = (int32_t)P->btasks.size();

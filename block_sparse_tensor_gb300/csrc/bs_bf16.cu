@@ -12,9 +12,9 @@
 // everything past a view's edge with zeros, so ragged d_k needs no padding in
 // memory and adds nothing.
 //
-// Warp roles (320 threads, one CTA per SM, tasks striped over CTAs in
-// longest-first order; each CTA's first task descriptors are preloaded to
-// shared memory in one round trip):
+// Warp roles (320 threads, one CTA per SM; each CTA runs its own task list,
+// built at plan time longest-first onto the least loaded CTA, and preloads
+// its first task descriptors to shared memory in one round trip):
 //   warp 0  TMA producer: A box (128 * kBf16MaxHalves) x 64 (K-major,
 //           128-byte swizzle) and B boxes 64 x 64 (N-major, 128-byte swizzle);
 //   warp 1  TMEM owner and MMA issuer (one thread): per 16-wide K step one
@@ -178,8 +178,9 @@ __device__ __forceinline__ void record_timeout(const Bf16Params &p, Ctl *ctl) {
   atomicExch(p.status, (int32_t)DS_TIMEOUT);
 }
 
-__device__ __forceinline__ Bf16Task task_at(const Bf16Params &p, const Bf16Task *cache, int ti, int t) {
-  return ti < kTaskCache ? cache[ti] : p.tasks[t];
+// The ti-th task of this CTA's list (the first kTaskCache come from shared memory).
+__device__ __forceinline__ Bf16Task task_at(const Bf16Params &p, const Bf16Task *cache, int beg, int ti) {
+  return ti < kTaskCache ? cache[ti] : p.tasks[p.cta_items[beg + ti]];
 }
 
 __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf16Params p) {
@@ -214,10 +215,9 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   // the epilogue warps preload this CTA's first task descriptors in one round trip
-  for (int i = threadIdx.x - 64; i >= 0 && i < kTaskCache; i += kThreadsBf16 - 64) {
-    const int t = blockIdx.x + i * gridDim.x;
-    if (t < p.ntasks) cache[i] = p.tasks[t];
-  }
+  const int my_beg = p.cta_ptr[blockIdx.x], my_n = p.cta_ptr[blockIdx.x + 1] - my_beg;
+  for (int i = threadIdx.x - 64; i >= 0 && i < kTaskCache; i += kThreadsBf16 - 64)
+    if (i < my_n) cache[i] = p.tasks[p.cta_items[my_beg + i]];
   fence_before();
   __syncthreads();
   fence_after();
@@ -230,12 +230,11 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       uint32_t phase = 0;
       bool ok = true;
       uint32_t outstanding = 0, issued_phase = 0;   // bit s: stage s has a copy in flight / its phase
-      if (blockIdx.x < p.ntasks) prefetch_task_maps(p, maps, cache[0]);
-      int ti = 0;
-      for (int t = blockIdx.x; ok && t < p.ntasks; t += gridDim.x, ++ti) {
-        const Bf16Task T = task_at(p, cache, ti, t);
-        if (t + (int)gridDim.x < p.ntasks)   // the next task's descriptors load while this one streams
-          prefetch_task_maps(p, maps, task_at(p, cache, ti + 1, t + gridDim.x));
+      if (my_n > 0) prefetch_task_maps(p, maps, cache[0]);
+      for (int ti = 0; ok && ti < my_n; ++ti) {
+        const Bf16Task T = task_at(p, cache, my_beg, ti);
+        if (ti + 1 < my_n)   // the next task's descriptors load while this one streams
+          prefetch_task_maps(p, maps, task_at(p, cache, my_beg, ti + 1));
         const int nb = (T.bn + 63) / 64;
         const uint32_t bytes = kATileBytes + nb * kBChunkBytes;
         for (int q = 0; ok && q < T.pair_count; ++q) {
@@ -294,9 +293,8 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       uint32_t te0 = 0, te1 = 0;   // tempty phase per slot
       bool ok = true;
       bool issued_any = false;
-      int ti = 0;
-      for (int t = blockIdx.x; ok && t < p.ntasks; t += gridDim.x, ++ti) {
-        const Bf16Task T = task_at(p, cache, ti, t);
+      for (int ti = 0; ok && ti < my_n; ++ti) {
+        const Bf16Task T = task_at(p, cache, my_beg, ti);
         const uint32_t idesc = instr_desc(T.bn);
         const bool two = T.mh == 2;
         const int s0 = two ? 0 : rot;
@@ -369,9 +367,8 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
     unsigned char *stg = epi_base + (size_t)ew * kEpiBufBytes;
     int rot = 0;
     uint32_t tf0 = 0, tf1 = 0;   // tfull phase per slot
-    int ti = 0;
-    for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x, ++ti) {
-      const Bf16Task T = task_at(p, cache, ti, t);
+    for (int ti = 0; ti < my_n; ++ti) {
+      const Bf16Task T = task_at(p, cache, my_beg, ti);
       const bool two = T.mh == 2;
       const int s0 = two ? 0 : rot;
       if (!two) rot ^= 1;

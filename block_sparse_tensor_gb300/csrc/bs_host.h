@@ -65,6 +65,8 @@ int fp64_max_ctas_per_sm();
 struct Bf16Params {
   const void *maps;        // CUtensorMap array in device memory (64-byte aligned)
   const Bf16Task *tasks;
+  const int32_t *cta_ptr;  // CTA b runs tasks cta_items[cta_ptr[b] .. cta_ptr[b+1]) in order
+  const int32_t *cta_items;
   const Bf16Pair *pairs;
   float *C;
   int32_t ntasks;

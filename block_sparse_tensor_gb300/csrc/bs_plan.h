@@ -74,6 +74,7 @@ struct bs_plan {
   std::vector<bs::ZeroBlock> zero_blocks;
   // BF16 path
   std::vector<bs::Bf16Task> btasks;
+  std::vector<int32_t> bcta_ptr, bcta_items;   // per-CTA task lists (longest first onto the least loaded CTA)
   std::vector<bs::Bf16Pair> bpairs;
   std::vector<bs::MapDesc> maps;
   std::vector<unsigned char> map_bytes;   // encoded maps (128 bytes each)
@@ -95,6 +96,8 @@ struct bs_plan {
   bs::PackCopy *d_pack = nullptr;
   bs::ZeroBlock *d_zero = nullptr;
   bs::Bf16Task *d_btasks = nullptr;
+  int32_t *d_bcta_ptr = nullptr;
+  int32_t *d_bcta_items = nullptr;
   bs::Bf16Pair *d_bpairs = nullptr;
   void *d_maps = nullptr;
   void *d_ws_a = nullptr, *d_ws_b = nullptr;
