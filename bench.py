@@ -326,7 +326,41 @@ def per_config(bs, torch, flush, stream, calib, peaks, args, clock_mhz):
         log(f"[bench] config {n}: {json.dumps(rec)}")
         del pb
         torch.cuda.empty_cache()
+    out["chain"] = chain_record(bs, torch, flush, stream)
+    log(f"[bench] chain: {json.dumps(out['chain'])}")
     return out
+
+
+def chain_record(bs, torch, flush, stream):
+    """Two chained contractions T = A B (free axis), Y = T D (contraction axis), T on the device."""
+    w1, w2 = bsgen.chain2()
+    A = bs.Layout(w1.rows, w1.inner, w1.rule_a, w1.layout_a, 8)
+    B = bs.Layout(w1.inner, w1.cols, w1.rule_b, w1.layout_b, 8)
+    P1 = bs.Plan(A, B, bs.F64, axis_policy=bs.AXIS_FREE, c_layout_flags=w1.layout_c)
+    D = bs.Layout(w2.inner, w2.cols, w2.rule_b, w2.layout_b, 8)
+    P2 = bs.Plan(P1.c_layout, D, bs.F64, axis_policy=bs.AXIS_CONTRACTION, c_layout_flags=w2.layout_c)
+
+    def dev(w, op, L):
+        b = L.blocks()
+        buf = np.zeros(L.nelems)
+        buf[L.element_index(b)] = w.draw(op, b[:, 0], b[:, 1], b[:, 3], b[:, 4])
+        return torch.from_numpy(buf).cuda()
+
+    a, b, d = dev(w1, 0, A), dev(w1, 1, B), dev(w2, 1, D)
+    t = torch.zeros(P1.c_layout.nelems, dtype=torch.float64, device="cuda")
+    y = torch.zeros(P2.c_layout.nelems, dtype=torch.float64, device="cuda")
+
+    def step():
+        bs.contract(P1, a, b, t, stream)
+        bs.contract(P2, t, d, y, stream)
+
+    ms = statistics.median(time_steps(torch, step, 20, 3, flush, stream))
+    s1, s2 = P1.stats(), P2.stats()
+    fl = s1["useful_flops"] + s2["useful_flops"]
+    return {"workload": "chain " + w1.name + " -> " + w2.name, "ms": ms, "gflops": fl / (ms * 1e-3) / 1e9,
+            "stage_axes": ["free", "contraction"], "launches": s1["launches"] + s2["launches"],
+            "useful_gflop": fl / 1e9, "triples": s1["triples"] + s2["triples"],
+            "roofline_frac": fl / (ms * 1e-3) / 1e12 / (NOMINAL_SMS * FP64_FLOP_PER_CLK_PER_SM * NOMINAL_MAX_MHZ * 1e6 / 1e12)}
 
 
 # ------------------------------------------------------------------------- CPU oracle

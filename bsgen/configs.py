@@ -215,3 +215,22 @@ def tiny_random(seed: int, values: str = "int3", max_sectors: int = 12, max_dim:
 
     return Workload(f"tiny_random_{seed}", dtype, axis(), axis(), axis(), rule(), rule(), values,
                     0x7E570000 + seed)
+
+
+def chain2():
+    """A two-stage chain shaped like the R/A/B/C apply: T = A B, then Y = T D.
+
+    Stage 1 is the 31-sector tail workload; D maps its column axis to an output
+    axis of the same 31 charges with |dq| <= 1 and N(0,1) values.  Returns the
+    stage-1 workload and the stage-2 workload whose `rows`/`inner` are T's axes
+    and whose rule_b / values describe D (its rule_a is unused: stage 2's
+    left operand is T, whose blocks are stage 1's structural product)."""
+    w1 = config2()
+    w1.layout_c = "rowpanel|charge_sorted"     # T is laid out for the next stage
+    qs = np.arange(-15, 16)
+    d = _dims(qs, lambda q: max(1, _round_half_away(64 * math.exp(-q * q / 50))))
+    out = Axis(qs, d)
+    w2 = Workload("chain_stage2_31x31x31", "f64", w1.rows, w1.cols, out, Rule(-100, 100), Rule(-1, 1),
+                  "normal", 0x5EED0000 + 102, layout_a="rowpanel|charge_sorted",
+                  layout_b="colpanel|charge_sorted", layout_c="blockrow")
+    return w1, w2

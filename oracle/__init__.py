@@ -187,3 +187,18 @@ def block_view(buf: np.ndarray, lay: Layout, r: int, c: int) -> np.ndarray:
     nr, nc = lay.rows[r], lay.cols[c]
     idx = off + np.arange(nr)[:, None] * ld + np.arange(nc)[None, :]
     return buf[idx]
+
+
+def chain_stage2(pr1: Problem, T: np.ndarray, w2, lb_flags=None, lc_flags=None) -> Problem:
+    """Second stage of a chain Y = T D, T being stage 1's C (values in stage 1's C layout).
+
+    T's populated blocks are stage 1's structural product; D follows w2's rule_b
+    and values (drawn as operand 1 of w2).  The contraction is the same plain
+    per-triple sum ("Two coalescing modes" does not change what is computed).
+    """
+    ma = pr1.mc
+    mb = rule_mask(w2.inner, w2.cols, w2.rule_b)
+    mc = product_mask(ma, mb)
+    B, lb = operand(w2, 1, w2.inner, w2.cols, mb, lb_flags or w2.layout_b)
+    lc = layout(w2.rows, w2.cols, mc, lc_flags or w2.layout_c, 8)
+    return Problem(w2, ma, mb, mc, pr1.lc, lb, lc, T, B)

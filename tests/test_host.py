@@ -218,3 +218,19 @@ def test_empty_structure():
     P = bs.Plan(A, B, bs.F64, host_only=1)
     st = P.stats()
     assert st["triples"] == 0 and st["c_blocks"] == 0 and P.c_layout.nelems == 0
+
+
+def test_chain_stage2_plans_on_stage1_c_layout():
+    """A plan's C layout serves as the next plan's A layout (per-stage axis choice)."""
+    w1, w2 = bsgen.chain2()
+    A = bs.Layout(w1.rows, w1.inner, w1.rule_a, w1.layout_a, 8)
+    B = bs.Layout(w1.inner, w1.cols, w1.rule_b, w1.layout_b, 8)
+    P1 = bs.Plan(A, B, bs.F64, host_only=1, axis_policy=bs.AXIS_FREE, c_layout_flags=w1.layout_c)
+    D = bs.Layout(w2.inner, w2.cols, w2.rule_b, w2.layout_b, 8)
+    P2 = bs.Plan(P1.c_layout, D, bs.F64, host_only=1, axis_policy=bs.AXIS_CONTRACTION, c_layout_flags=w2.layout_c)
+    s1, s2 = P1.stats(), P2.stats()
+    assert s1["axis"] == bs.AXIS_FREE and s2["axis"] == bs.AXIS_CONTRACTION
+    pr1 = oracle.problem(w1)
+    assert s2["c_blocks"] == int(oracle.product_mask(pr1.mc, oracle.rule_mask(w2.inner, w2.cols, w2.rule_b)).sum())
+    # T in charge-sorted row panels makes every stage-2 group one view
+    assert np.all(P2.groups()[:, 5] == 1)

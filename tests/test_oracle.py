@@ -301,3 +301,25 @@ def test_planted_mistake_is_caught(name):
         assert fails, f"planted mistake {name} went unnoticed"
     finally:
         shutil.rmtree(tmp, ignore_errors=True)
+
+
+def test_chain_matches_dense_triple_product():
+    """The two-stage chain Y = (A B) D equals the dense product of the three embeddings."""
+    w1, w2 = bsgen.chain2()
+    pr1 = oracle.problem(w1)
+    T, _ = oracle.contract(pr1)
+    pr2 = oracle.chain_stage2(pr1, T, w2)
+    Y, S = oracle.contract(pr2)
+    DA, ri, ki = dense_operand(w1, 0, w1.rows, w1.inner, w1.rule_a)
+    DB, _, cj = dense_operand(w1, 1, w1.inner, w1.cols, w1.rule_b)
+    DD, _, oj = dense_operand(w2, 1, w2.inner, w2.cols, w2.rule_b)
+    DY = (DA @ DB) @ DD
+    for i in range(w2.rows.n):
+        for j in range(w2.cols.n):
+            ref = DY[ri[i]:ri[i + 1], oj[j]:oj[j + 1]]
+            if not pr2.mc[i, j]:
+                assert np.all(ref == 0.0)
+                continue
+            got = oracle.block_view(Y, pr2.lc, i, j)
+            s = oracle.block_view(S, pr2.lc, i, j)
+            assert np.linalg.norm(got - ref) <= 1e-13 * max(np.linalg.norm(s), 1e-300)
