@@ -175,13 +175,13 @@ void build_bf16(bs_plan *P) {
     for (int32_t s = 0; s < g.kseg_count; ++s) {
       const KSeg &k = gs.ksegs[g.kseg_begin + s];
       Bf16Pair pr{};
-      pr.map_a = map_id(0, k.ka, k.klen, g.m, k.kl, 64, 128 * kBf16MaxHalves);
+      pr.map_a = map_id(0, k.ka, k.klen, g.m, k.kl, 64, 128);
       pr.map_b = map_id(1, k.kb, g.n, k.klen, k.ldb, 64, 64);
       pr.klen = k.klen;
       P->bpairs.push_back(pr);
     }
-    // tiles of kBf16MaxHalves x 128 rows; two halves share each B tile
-    for (int32_t m0 = 0; m0 < g.m; m0 += 128 * kBf16MaxHalves)
+    // 128-row tiles, up to 256 columns wide
+    for (int32_t m0 = 0; m0 < g.m; m0 += 128)
       for (int32_t n0 = 0; n0 < g.n; n0 += 256) {
         Bf16Task t{};
         t.pair_begin = pb;
@@ -191,13 +191,12 @@ void build_bf16(bs_plan *P) {
         t.m = g.m;
         t.n = g.n;
         t.bn = (std::min(256, g.n - n0) + 15) / 16 * 16;
-        t.mh = (int16_t)(kBf16MaxHalves == 2 && g.m - m0 > 128 ? 2 : 1);
         t.c_off = rs.rc;
         t.ldc = rs.ldc;
-        t.c_vec = (int16_t)(tma_ok(rs.rc, rs.ldc, 4) ? 1 : 0);   // 16-byte aligned rows: vector stores
+        t.c_vec = tma_ok(rs.rc, rs.ldc, 4) ? 1 : 0;   // 16-byte aligned rows: vector stores
         int64_t kch = 0;
         for (int32_t s = 0; s < g.kseg_count; ++s) kch += (gs.ksegs[g.kseg_begin + s].klen + 63) / 64;
-        costed.push_back({(double)kch * (t.bn * t.mh + 64), t});
+        costed.push_back({(double)kch * (t.bn + 64), t});
       }
   }
   std::stable_sort(costed.begin(), costed.end(),
@@ -215,14 +214,40 @@ void build_bf16(bs_plan *P) {
     int64_t st = 0;
     for (int32_t q = 0; q < T.pair_count; ++q) st += (P->bpairs[T.pair_begin + q].klen + 63) / 64;
     std::pop_heap(heap.begin(), heap.end(), cmp);
-    heap.back().first += 150.0 + (double)st * (96.0 + T.bn * T.mh);
+    heap.back().first += 150.0 + (double)st * (96.0 + T.bn);
     lists[heap.back().second].push_back((int32_t)t);
     std::push_heap(heap.begin(), heap.end(), cmp);
   }
-  P->bcta_ptr.assign(ncta + 1, 0);
+  // Unroll every CTA's list into tasks and 64-deep K stages, in execution order.
+  P->bctas.assign(ncta, Bf16Cta{});
   for (int c = 0; c < ncta; ++c) {
-    P->bcta_items.insert(P->bcta_items.end(), lists[c].begin(), lists[c].end());
-    P->bcta_ptr[c + 1] = (int32_t)P->bcta_items.size();
+    Bf16Cta &cd = P->bctas[c];
+    cd.task_begin = (int32_t)P->bstasks.size();
+    cd.stage_begin = (int32_t)P->bstages.size();
+    for (int32_t t : lists[c]) {
+      const Bf16Task &T = P->btasks[t];
+      P->bstasks.push_back(T);
+      const size_t first = P->bstages.size();
+      for (int32_t q = 0; q < T.pair_count; ++q) {
+        const Bf16Pair &pr = P->bpairs[T.pair_begin + q];
+        for (int32_t k0 = 0; k0 < pr.klen; k0 += 64) {
+          Bf16Stage e{};
+          e.map_a = pr.map_a;
+          e.map_b = pr.map_b;
+          e.k0 = k0;
+          e.m0 = T.m0;
+          e.n0 = T.n0;
+          e.nb = (int16_t)((T.bn + 63) / 64);
+          e.ksteps = (int16_t)std::min(4, (pr.klen - k0 + 15) / 16);
+          e.bn = (int16_t)T.bn;
+          P->bstages.push_back(e);
+        }
+      }
+      P->bstages[first].flags |= kStageFirst;
+      P->bstages.back().flags |= kStageLast;
+    }
+    cd.task_count = (int32_t)P->bstasks.size() - cd.task_begin;
+    cd.stage_count = (int32_t)P->bstages.size() - cd.stage_begin;
   }
 }
 
@@ -237,10 +262,9 @@ bs_status upload(bs_plan *P) {
   size_t o_tqi = append_bytes(buf, P->ts.tq_items);
   size_t o_pack = append_bytes(buf, P->pack_copies);
   size_t o_zero = append_bytes(buf, P->zero_blocks);
-  size_t o_bt = append_bytes(buf, P->btasks);
-  size_t o_bp = append_bytes(buf, P->bpairs);
-  size_t o_bcp = append_bytes(buf, P->bcta_ptr);
-  size_t o_bci = append_bytes(buf, P->bcta_items);
+  size_t o_bc = append_bytes(buf, P->bctas);
+  size_t o_bt = append_bytes(buf, P->bstasks);
+  size_t o_bs = append_bytes(buf, P->bstages);
   std::vector<unsigned char> mapspace(P->maps.size() * sizeof(CUtensorMap), 0);
   size_t o_maps = append_bytes(buf, mapspace);
   size_t total = (buf.size() + 255) / 256 * 256 + 256;
@@ -258,10 +282,9 @@ bs_status upload(bs_plan *P) {
   P->d_tq_items = (int32_t *)(b + o_tqi);
   P->d_pack = (PackCopy *)(b + o_pack);
   P->d_zero = (ZeroBlock *)(b + o_zero);
-  P->d_btasks = (Bf16Task *)(b + o_bt);
-  P->d_bcta_ptr = (int32_t *)(b + o_bcp);
-  P->d_bcta_items = (int32_t *)(b + o_bci);
-  P->d_bpairs = (Bf16Pair *)(b + o_bp);
+  P->d_bctas = (Bf16Cta *)(b + o_bc);
+  P->d_bstasks = (Bf16Task *)(b + o_bt);
+  P->d_bstages = (Bf16Stage *)(b + o_bs);
   P->d_maps = (void *)(b + o_maps);
   // counters and status word: zero once, kernels return them to zero
   void *cs = nullptr;
@@ -563,7 +586,7 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
       for (const auto &t : P->btasks) {
         int64_t kk = 0;
         for (int32_t s = 0; s < t.pair_count; ++s) kk += (P->bpairs[t.pair_begin + s].klen + 15) / 16 * 16;
-        ex += 2.0 * 128 * t.mh * t.bn * kk;
+        ex += 2.0 * 128 * t.bn * kk;
       }
       S.executed_flops = ex;
     }
@@ -580,7 +603,7 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
         const int64_t work_items = (int64_t)P->ts.tasks.size() + (int64_t)(P->ts.tail_elems.size() / 2 + kThreads - 1) / kThreads;
         P->grid = (int)std::max<int64_t>(1, std::min<int64_t>(work_items, (int64_t)P->sm_count * cps));
       }
-      else P->grid = std::max(1, (int)P->bcta_ptr.size() - 1);
+      else P->grid = std::max(1, (int)P->bctas.size());
     }
   } catch (const std::bad_alloc &) {
     free_device(P);
@@ -690,12 +713,10 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
     }
     Bf16Params p{};
     p.maps = P->d_maps;
-    p.tasks = P->d_btasks;
-    p.cta_ptr = P->d_bcta_ptr;
-    p.cta_items = P->d_bcta_items;
-    p.pairs = P->d_bpairs;
+    p.ctas = P->d_bctas;
+    p.tasks = P->d_bstasks;
+    p.stages = P->d_bstages;
     p.C = (float *)C;
-    p.ntasks = (int32_t)P->btasks.size();
     p.status = P->d_status;
     p.counter = P->d_counter;
     p.timeout_ns = (uint64_t)(P->opts.wait_timeout_ms > 0 ? P->opts.wait_timeout_ms : 2000) * 1000000ull;

@@ -4,26 +4,27 @@
 // The tensor-core path is taken only where a coalesced group is a genuine
 // dense contraction in a type with a tensor-core path (uni20 design note
 // "block coalescing", "Two coalescing modes": a single-axis group is one
-// zero-waste GEMM).  One task is a (128 * mh) x BN tile (BN <= 256, mh = 1 by
-// default; mh = 2 puts two 128-row halves in two TMEM accumulators that share
-// every B tile) of one contraction-axis group.  The K loop walks the group's
-// inner segments, each with its own tensor maps for the A view (group rows x
-// d_k) and the B view (d_k x group columns).  The copy engine fills
-// everything past a view's edge with zeros, so ragged d_k needs no padding in
-// memory and adds nothing.
+// zero-waste GEMM).  One task is a 128 x BN tile (BN <= 256) of one
+// contraction-axis group.  Its K loop walks the group's inner segments, each
+// with its own tensor maps for the A view (group rows x d_k) and the B view
+// (d_k x group columns).  The copy engine fills everything past a view's edge
+// with zeros, so ragged d_k needs no padding in memory and adds nothing.
 //
-// Warp roles (320 threads, one CTA per SM; each CTA runs its own task list,
-// built at plan time longest-first onto the least loaded CTA, and preloads
-// its first task descriptors to shared memory in one round trip):
-//   warp 0  TMA producer: A box (128 * kBf16MaxHalves) x 64 (K-major,
-//           128-byte swizzle) and B boxes 64 x 64 (N-major, 128-byte swizzle);
-//   warp 1  TMEM owner and MMA issuer (one thread): per 16-wide K step one
-//           M128 x N=BN x K16 MMA per half, into 256-column FP32 slots used in
-//           rotation, so the epilogue of one tile overlaps the next tile;
+// One CTA per SM.  At plan time each CTA gets its own task list (longest
+// first onto the least loaded CTA), unrolled into a flat list of 64-deep K
+// stages; the CTA preloads the head of both lists to shared memory, so the
+// copy and MMA threads never wait on a table in global memory.
+//   warp 0  TMA producer (one thread): per stage one A box 128 x 64 (K-major,
+//           128-byte swizzle) and up to four B boxes 64 x 64 (N-major, 128-byte
+//           swizzle).  It fills the first ring of stages straight from the
+//           global list while the rest of the CTA is still setting up;
+//   warp 1  TMEM owner and MMA issuer (one thread): per stage up to four
+//           M128 x N=BN x K16 MMAs (one instruction block when all four reach
+//           real K) into 256-column FP32 slots used in rotation, so the
+//           epilogue of one tile overlaps the next tile's MMAs;
 //   warps 2-9  epilogue, two warps per 32-lane TMEM quarter: tcgen05.ld of 32
 //           columns at a time, a swizzled shared-memory transpose, coalesced
-//           masked stores (plain stores: the copy engine serves only loads,
-//           and no padding byte of C is written).
+//           masked stores (plain stores: no padding byte of C is written).
 // Every wait is bounded by the global timer; on expiry the kernel records
 // a timeout in the status word, drains its copies and MMAs (again bounded),
 // frees its tensor memory and returns.
@@ -35,11 +36,10 @@ namespace bs {
 
 namespace {
 
-constexpr int kStages = kBf16MaxHalves == 2 ? 3 : 4;
-constexpr int kBM = 128;                          // rows of one accumulator (UMMA M)
+constexpr int kStages = 4;
+constexpr int kBM = 128;                          // rows of the accumulator (UMMA M)
 constexpr int kBK = 64;                           // K per stage (one 128-byte swizzle row of BF16)
-constexpr int kAHalfBytes = kBM * kBK * 2;        // 16 KB: 128 rows of A
-constexpr int kATileBytes = kBf16MaxHalves * kAHalfBytes;   // one A box of 128 or 256 rows
+constexpr int kATileBytes = kBM * kBK * 2;        // 16 KB: 128 rows of A
 constexpr int kBChunkBytes = 64 * kBK * 2;        // one 64-column N chunk of B: 8 KB
 constexpr int kBTileBytes = 4 * kBChunkBytes;     // BN up to 256
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
@@ -47,7 +47,8 @@ constexpr int kTmemCols = 512;                    // two 256-column FP32 accumul
 constexpr int kEpiWarps = 8;                      // two epilogue warps per TMEM lane quarter
 constexpr int kThreadsBf16 = 64 + 32 * kEpiWarps;
 constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x 32 FP32 columns per epilogue warp
-constexpr int kTaskCache = 16;                    // this CTA's first tasks, preloaded to shared memory
+constexpr int kTaskCache = 16;                    // head of this CTA's task list, in shared memory
+constexpr int kStageCache = 32;                   // head of this CTA's stage list, in shared memory
 
 struct Ctl {
   uint64_t full[kStages];
@@ -59,9 +60,10 @@ struct Ctl {
   int32_t abort_flag;
 };
 
-constexpr int kCtlBytes = 256;                    // Ctl rounded up
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kEpiBufBytes +
-                              kCtlBytes + kTaskCache * sizeof(Bf16Task);
+// [control block | task cache | stage cache | pad to 1024 | stages | epilogue staging]
+constexpr int kCtlBytes = 256;
+constexpr int kHeadBytes = kCtlBytes + kTaskCache * (int)sizeof(Bf16Task) + kStageCache * (int)sizeof(Bf16Stage);
+constexpr size_t kSmemBytes = kHeadBytes + 1023 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kEpiBufBytes;
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
@@ -113,15 +115,6 @@ __device__ __forceinline__ void prefetch_map(const void *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
-// Warm the descriptor cache with every tensor map a task will use.
-__device__ __forceinline__ void prefetch_task_maps(const Bf16Params &p, const char *maps, const Bf16Task &T) {
-  for (int q = 0; q < T.pair_count; ++q) {
-    const Bf16Pair pr = p.pairs[T.pair_begin + q];
-    prefetch_map(maps + (size_t)pr.map_a * 128);
-    prefetch_map(maps + (size_t)pr.map_b * 128);
-  }
-}
-
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint32_t mbar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
@@ -146,6 +139,23 @@ __device__ __forceinline__ uint32_t instr_desc(int n) {
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// The four K16 steps of a full stage in one instruction block: the shared
+// memory descriptors advance by 32 bytes of A (2 units) and 2048 bytes of B
+// (128 units) per step, so only the first MMA of a tile starts from zero.
+__device__ __forceinline__ void mma_bf16_x4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b64 a1, a2, a3, b1, b2, b3;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, 0, 0;\n"
+      " add.s64 a1, %1, 2;\n add.s64 a2, %1, 4;\n add.s64 a3, %1, 6;\n"
+      " add.s64 b1, %2, 128;\n add.s64 b2, %2, 256;\n add.s64 b3, %2, 384;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
@@ -178,21 +188,50 @@ __device__ __forceinline__ void record_timeout(const Bf16Params &p, Ctl *ctl) {
   atomicExch(p.status, (int32_t)DS_TIMEOUT);
 }
 
-// The ti-th task of this CTA's list (the first kTaskCache come from shared memory).
-__device__ __forceinline__ Bf16Task task_at(const Bf16Params &p, const Bf16Task *cache, int beg, int ti) {
-  return ti < kTaskCache ? cache[ti] : p.tasks[p.cta_items[beg + ti]];
+// The ti-th task and the si-th stage of this CTA's lists (the heads come from shared memory).
+__device__ __forceinline__ Bf16Task task_at(const Bf16Params &p, const Bf16Task *cache, const Bf16Cta &me, int ti) {
+  return ti < kTaskCache ? cache[ti] : p.tasks[me.task_begin + ti];
+}
+__device__ __forceinline__ Bf16Stage stage_at(const Bf16Params &p, const Bf16Stage *cache, const Bf16Cta &me, int si) {
+  return si < kStageCache ? cache[si] : p.stages[me.stage_begin + si];
 }
 
 __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf16Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // [stages | epilogue staging, 1024-aligned for the 128-byte swizzle | control block | task cache]
+  Ctl *ctl = (Ctl *)smem_raw;
+  Bf16Task *tcache = (Bf16Task *)(smem_raw + kCtlBytes);
+  Bf16Stage *scache = (Bf16Stage *)(smem_raw + kCtlBytes + kTaskCache * sizeof(Bf16Task));
+  // stage buffers 1024-aligned for the 128-byte swizzle
+  unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + kHeadBytes + 1023) & ~(uintptr_t)1023);
   unsigned char *epi_base = smem + (size_t)kStages * kStageBytes;
-  Ctl *ctl = (Ctl *)(epi_base + (size_t)kEpiWarps * kEpiBufBytes);
-  Bf16Task *cache = (Bf16Task *)((unsigned char *)ctl + kCtlBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int32_t *abort_flag = &ctl->abort_flag;
   const char *maps = (const char *)p.maps;
+  const Bf16Cta me = p.ctas[blockIdx.x];
+
+  // producer state (thread 0 only)
+  int ps = 0, pstage = 0;
+  uint32_t pphase = 0;
+  uint32_t outstanding = 0, issued_phase = 0;   // bit s: stage s has a copy in flight / its phase
+  auto issue = [&](const Bf16Stage &E) {
+    const uint32_t fb = smem_u32(&ctl->full[pstage]);
+    // test hook: CTA 0's first stage is never filled, so the MMA thread's
+    // bounded wait on it runs out and the kernel reports a timeout
+    const bool withhold = (p.debug_flags & 1) && blockIdx.x == 0 && ps == 0;
+    if (!withhold) {
+      mbar_expect_tx(fb, (uint32_t)(kATileBytes + E.nb * kBChunkBytes));
+      unsigned char *st = smem + (size_t)pstage * kStageBytes;
+      tma_load_2d(smem_u32(st), maps + (size_t)E.map_a * 128, fb, E.k0, E.m0);   // rows past the group read as zero
+      const void *mb = maps + (size_t)E.map_b * 128;
+      for (int c = 0; c < E.nb; ++c) tma_load_2d(smem_u32(st + kATileBytes + c * kBChunkBytes), mb, fb, E.n0 + 64 * c, E.k0);
+      outstanding |= 1u << pstage;
+      issued_phase = (issued_phase & ~(1u << pstage)) | (pphase << pstage);
+    }
+    if (++pstage == kStages) {
+      pstage = 0;
+      pphase ^= 1u;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -207,6 +246,9 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
     ctl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    // The first ring of stages needs no free slot: fill it from the global
+    // list while the other warps allocate tensor memory and load the lists.
+    for (const int n = min(kStages, me.stage_count); ps < n; ++ps) issue(p.stages[me.stage_begin + ps]);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&ctl->tmem_base)),
@@ -214,10 +256,12 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // the epilogue warps preload this CTA's first task descriptors in one round trip
-  const int my_beg = p.cta_ptr[blockIdx.x], my_n = p.cta_ptr[blockIdx.x + 1] - my_beg;
-  for (int i = threadIdx.x - 64; i >= 0 && i < kTaskCache; i += kThreadsBf16 - 64)
-    if (i < my_n) cache[i] = p.tasks[p.cta_items[my_beg + i]];
+  if (threadIdx.x >= 64) {   // the epilogue warps preload the heads of both lists
+    const int i = threadIdx.x - 64;
+    if (i < kTaskCache && i < me.task_count) tcache[i] = p.tasks[me.task_begin + i];
+    const int j = i - 64;
+    if (j >= 0 && j < kStageCache && j < me.stage_count) scache[j] = p.stages[me.stage_begin + j];
+  }
   fence_before();
   __syncthreads();
   fence_after();
@@ -226,49 +270,17 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      uint32_t outstanding = 0, issued_phase = 0;   // bit s: stage s has a copy in flight / its phase
-      if (my_n > 0) prefetch_task_maps(p, maps, cache[0]);
-      for (int ti = 0; ok && ti < my_n; ++ti) {
-        const Bf16Task T = task_at(p, cache, my_beg, ti);
-        if (ti + 1 < my_n)   // the next task's descriptors load while this one streams
-          prefetch_task_maps(p, maps, task_at(p, cache, my_beg, ti + 1));
-        const int nb = (T.bn + 63) / 64;
-        const uint32_t bytes = kATileBytes + nb * kBChunkBytes;
-        for (int q = 0; ok && q < T.pair_count; ++q) {
-          const Bf16Pair pr = p.pairs[T.pair_begin + q];
-          const void *ma = maps + (size_t)pr.map_a * 128;
-          const void *mb = maps + (size_t)pr.map_b * 128;
-          for (int kc = 0; kc < pr.klen; kc += kBK) {
-            if (!mbar_wait(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {
-              record_timeout(p, ctl);
-              ok = false;
-              break;
-            }
-            const uint32_t fb = smem_u32(&ctl->full[stage]);
-            if ((p.debug_flags & 1) && blockIdx.x == 0 && ti == 0 && q == 0 && kc == 0) {
-              // test hook: this stage is never filled, so the MMA thread's
-              // bounded wait on it runs out and the kernel reports a timeout
-              if (++stage == kStages) {
-                stage = 0;
-                phase ^= 1u;
-              }
-              continue;
-            }
-            mbar_expect_tx(fb, bytes);
-            unsigned char *st = smem + (size_t)stage * kStageBytes;
-            tma_load_2d(smem_u32(st), ma, fb, kc, T.m0);   // rows past the group read as zero
-            for (int c = 0; c < nb; ++c)
-              tma_load_2d(smem_u32(st + kATileBytes + c * kBChunkBytes), mb, fb, T.n0 + 64 * c, kc);
-            outstanding |= 1u << stage;
-            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
+      for (; ps < me.stage_count; ++ps) {
+        const Bf16Stage E = stage_at(p, scache, me, ps);
+        if (!mbar_wait(smem_u32(&ctl->empty[pstage]), pphase ^ 1u, abort_flag, p.timeout_ns)) {
+          record_timeout(p, ctl);
+          break;
+        }
+        issue(E);
+        if (ps + 2 < me.stage_count) {   // warm the descriptor cache two stages ahead
+          const Bf16Stage F = stage_at(p, scache, me, ps + 2);
+          prefetch_map(maps + (size_t)F.map_a * 128);
+          prefetch_map(maps + (size_t)F.map_b * 128);
         }
       }
       // Drain: every issued stage completes its transfer before the CTA exits.
@@ -283,68 +295,51 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      // Accumulator slots: a two-half task uses both, a one-half task the next
-      // one in rotation; the epilogue walks the same sequence.  Everything the
-      // issue loop touches stays in scalar registers (a local array here cost
-      // more than half the tensor throughput).
-      int stage = 0;
-      uint32_t phase = 0;
-      int rot = 0;
-      uint32_t te0 = 0, te1 = 0;   // tempty phase per slot
-      bool ok = true;
+      // Tiles take the two accumulator slots in turn; the epilogue walks the
+      // same sequence.  Everything the issue loop touches stays in scalar
+      // registers (a local array here cost more than half the tensor
+      // throughput), and a full stage is one instruction block.
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, te0 = 0, te1 = 0;   // ring phase; tempty phase per slot
+      uint32_t d = tmem_base, idesc = 0, acc = 0;
       bool issued_any = false;
-      for (int ti = 0; ok && ti < my_n; ++ti) {
-        const Bf16Task T = task_at(p, cache, my_beg, ti);
-        const uint32_t idesc = instr_desc(T.bn);
-        const bool two = T.mh == 2;
-        const int s0 = two ? 0 : rot;
-        if (!two) rot ^= 1;
-        if (!mbar_wait(smem_u32(&ctl->tempty[s0]), (s0 ? te1 : te0) ^ 1u, abort_flag, p.timeout_ns)) {
-          record_timeout(p, ctl);
-          break;
-        }
-        if (s0) te1 ^= 1u;
-        else te0 ^= 1u;
-        if (two) {
-          if (!mbar_wait(smem_u32(&ctl->tempty[1]), te1 ^ 1u, abort_flag, p.timeout_ns)) {
+      for (int si = 0; si < me.stage_count; ++si) {
+        const Bf16Stage E = stage_at(p, scache, me, si);
+        if (E.flags & kStageFirst) {
+          if (!mbar_wait(smem_u32(&ctl->tempty[slot]), (slot ? te1 : te0) ^ 1u, abort_flag, p.timeout_ns)) {
             record_timeout(p, ctl);
             break;
           }
-          te1 ^= 1u;
+          if (slot) te1 ^= 1u;
+          else te0 ^= 1u;
+          fence_after();
+          d = tmem_base + (uint32_t)(slot * 256);
+          idesc = instr_desc(E.bn);
+          acc = 0;
+        }
+        if (!mbar_wait(smem_u32(&ctl->full[stage]), phase, abort_flag, p.timeout_ns)) {
+          record_timeout(p, ctl);
+          break;
         }
         fence_after();
-        const uint32_t d0 = tmem_base + (uint32_t)(s0 * 256);
-        const uint32_t d1 = tmem_base + 256u;
-        uint32_t accumulate = 0;
-        for (int q = 0; ok && q < T.pair_count; ++q) {
-          const int klen = p.pairs[T.pair_begin + q].klen;
-          for (int kc = 0; kc < klen; kc += kBK) {
-            if (!mbar_wait(smem_u32(&ctl->full[stage]), phase, abort_flag, p.timeout_ns)) {
-              record_timeout(p, ctl);
-              ok = false;
-              break;
-            }
-            fence_after();
-            const uint32_t a0 = smem_u32(smem + (size_t)stage * kStageBytes);
-            const uint32_t b0 = a0 + kATileBytes;
-            const int ksteps = min(4, (klen - kc + 15) / 16);
-            for (int ks = 0; ks < ksteps; ++ks) {
-              const uint64_t bd = smem_desc(b0 + ks * 2048, kBChunkBytes, 1024);
-              mma_bf16(d0, smem_desc(a0 + ks * 32, 16, 1024), bd, idesc, accumulate);
-              if (two) mma_bf16(d1, smem_desc(a0 + kAHalfBytes + ks * 32, 16, 1024), bd, idesc, accumulate);
-              accumulate = 1;
-            }
-            mma_commit(smem_u32(&ctl->empty[stage]));
-            issued_any = true;
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
+        const uint32_t a0 = smem_u32(smem + (size_t)stage * kStageBytes);
+        const uint64_t ad = smem_desc(a0, 16, 1024), bd = smem_desc(a0 + kATileBytes, kBChunkBytes, 1024);
+        if (E.ksteps == 4) {
+          mma_bf16_x4(d, ad, bd, idesc, acc);
+        } else {
+          for (int ks = 0; ks < E.ksteps; ++ks) mma_bf16(d, ad + 2 * ks, bd + 128 * ks, idesc, acc | (uint32_t)ks);
         }
-        if (!ok) break;
-        mma_commit(smem_u32(&ctl->tfull[s0]));
-        if (two) mma_commit(smem_u32(&ctl->tfull[1]));
+        acc = 1;
+        mma_commit(smem_u32(&ctl->empty[stage]));
+        issued_any = true;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (E.flags & kStageLast) {
+          mma_commit(smem_u32(&ctl->tfull[slot]));
+          slot ^= 1;
+        }
       }
       // Drain: all MMAs issued by this thread finish before tensor memory is freed.
       if (issued_any) {
@@ -363,36 +358,24 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
     // of four 128-byte row segments per instruction, masked at the group edge.
     const int quarter = warp & 3;
     const int ew = warp - 2;
-    const int grp = ew >> 2;                  // 0 or 1: which half (two-half tasks) or which chunks
+    const int grp = ew >> 2;                  // 0 or 1: which 32-column chunks
     unsigned char *stg = epi_base + (size_t)ew * kEpiBufBytes;
-    int rot = 0;
+    int slot = 0;
     uint32_t tf0 = 0, tf1 = 0;   // tfull phase per slot
-    for (int ti = 0; ti < my_n; ++ti) {
-      const Bf16Task T = task_at(p, cache, my_beg, ti);
-      const bool two = T.mh == 2;
-      const int s0 = two ? 0 : rot;
-      if (!two) rot ^= 1;
-      if (!mbar_wait(smem_u32(&ctl->tfull[s0]), s0 ? tf1 : tf0, abort_flag, p.timeout_ns)) {
+    for (int ti = 0; ti < me.task_count; ++ti) {
+      const Bf16Task T = task_at(p, tcache, me, ti);
+      if (!mbar_wait(smem_u32(&ctl->tfull[slot]), slot ? tf1 : tf0, abort_flag, p.timeout_ns)) {
         if (lane == 0) record_timeout(p, ctl);
         break;
       }
-      if (s0) tf1 ^= 1u;
+      if (slot) tf1 ^= 1u;
       else tf0 ^= 1u;
-      if (two) {
-        if (!mbar_wait(smem_u32(&ctl->tfull[1]), tf1, abort_flag, p.timeout_ns)) {
-          if (lane == 0) record_timeout(p, ctl);
-          break;
-        }
-        tf1 ^= 1u;
-      }
       fence_after();
-      const int my_slot = two ? grp : s0;
-      const int row0 = T.m0 + (two ? 128 * grp : 0) + 32 * quarter;
-      const int c_first = two ? 0 : 32 * grp, c_step = two ? 32 : 64;
+      const int row0 = T.m0 + 32 * quarter;
       if (row0 < T.m) {
-        const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(my_slot * 256);
+        const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(slot * 256);
         float *cbase = p.C + T.c_off;
-        for (int c0 = c_first; c0 < T.bn; c0 += c_step) {
+        for (int c0 = 32 * grp; c0 < T.bn; c0 += 64) {
           float v[32];
           tmem_ld32(trow + c0, v);
           unsigned char *mine = stg + lane * 128;
@@ -424,10 +407,8 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       }
       fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&ctl->tempty[s0]));
-        if (two) mbar_arrive(smem_u32(&ctl->tempty[1]));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[slot]));
+      slot ^= 1;
     }
   }
   fence_before();

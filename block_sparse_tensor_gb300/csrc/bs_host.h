@@ -63,19 +63,16 @@ cudaError_t launch_control_bf16(const uint16_t *A, const uint16_t *B, float *C, 
 int fp64_max_ctas_per_sm();
 
 struct Bf16Params {
-  const void *maps;        // CUtensorMap array in device memory (64-byte aligned)
-  const Bf16Task *tasks;
-  const int32_t *cta_ptr;  // CTA b runs tasks cta_items[cta_ptr[b] .. cta_ptr[b+1]) in order
-  const int32_t *cta_items;
-  const Bf16Pair *pairs;
+  const void *maps;          // CUtensorMap array in device memory (64-byte aligned)
+  const Bf16Cta *ctas;       // CTA b runs tasks[ctas[b].task_begin ..] and stages[ctas[b].stage_begin ..]
+  const Bf16Task *tasks;     // per-CTA task lists, concatenated in execution order
+  const Bf16Stage *stages;   // per-CTA stage lists, concatenated in execution order
   float *C;
-  int32_t ntasks;
-  int32_t pad_;
   int32_t *status;
   uint32_t *counter;
   uint64_t timeout_ns;
   int32_t debug_flags;
-  int32_t pad2_;
+  int32_t pad_;
 };
 cudaError_t launch_bf16_grouped(const Bf16Params &p, int grid, cudaStream_t s);
 size_t bf16_smem_bytes();

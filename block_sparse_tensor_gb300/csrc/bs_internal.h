@@ -135,11 +135,10 @@ struct PackParams {
 };
 
 // ---- BF16 tensor-core path ------------------------------------------------
-// One task = a (128 * mh) x BN tile of a contraction-axis group (mh = 1 or 2
-// row halves, each with its own TMEM accumulator; both halves share every B
-// tile); its K loop walks the group's block pairs, each with its own tensor
-// maps (zero fill past the block edge keeps ragged K exact).
-constexpr int kBf16MaxHalves = 1;     // 128-row halves per BF16 tile (1: 128-row tiles, 2: 256-row tiles)
+// One task = a 128 x BN tile of a contraction-axis group; its K loop walks the
+// group's block pairs, each with its own tensor maps (zero fill past the block
+// edge keeps ragged K exact).  At plan time every CTA's tasks are unrolled into
+// a flat list of 64-deep K stages, so the copy and MMA threads only walk a list.
 
 struct Bf16Pair {
   int32_t map_a;   // index of the A tensor map (rows of the group x d_k)
@@ -156,10 +155,33 @@ struct Bf16Task {
   int32_t m;         // rows of the group
   int32_t n;         // columns of the group
   int32_t bn;        // UMMA N of the tile (multiple of 16, <= 256)
-  int16_t mh;        // 128-row halves in the tile: 1 or 2 (each its own TMEM accumulator)
-  int16_t c_vec;     // 1 when every C row of the group starts 16-byte aligned (vector stores)
+  int32_t c_vec;     // 1 when every C row of the group starts 16-byte aligned (vector stores)
   int64_t c_off;     // C offset of the group's (0, 0) element
   int64_t ldc;
+};
+
+// One K stage: an A box (128 rows x 64 K) and nb B boxes (64 K x 64 columns).
+constexpr int kStageFirst = 1;   // first stage of its tile: the accumulator starts from zero
+constexpr int kStageLast = 2;    // last stage of its tile: the accumulator is complete afterwards
+
+struct Bf16Stage {
+  int32_t map_a;
+  int32_t map_b;
+  int32_t k0;       // K coordinate of the stage inside the pair's views
+  int32_t m0;       // row coordinate of the A box
+  int32_t n0;       // column coordinate of the first B box
+  int16_t nb;       // B boxes (64 columns each)
+  int16_t ksteps;   // K16 MMA steps that reach real K (1..4)
+  int16_t bn;       // UMMA N of the tile
+  int16_t flags;    // kStageFirst | kStageLast
+  int32_t pad_;
+};
+static_assert(sizeof(Bf16Stage) == 32, "stage record");
+
+// This CTA's slice of the task and stage lists (both in execution order).
+struct Bf16Cta {
+  int32_t task_begin, task_count;
+  int32_t stage_begin, stage_count;
 };
 
 }  // namespace bs

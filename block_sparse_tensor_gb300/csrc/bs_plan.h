@@ -73,9 +73,11 @@ struct bs_plan {
   int32_t pack_copies_a = 0;
   std::vector<bs::ZeroBlock> zero_blocks;
   // BF16 path
-  std::vector<bs::Bf16Task> btasks;
-  std::vector<int32_t> bcta_ptr, bcta_items;   // per-CTA task lists (longest first onto the least loaded CTA)
+  std::vector<bs::Bf16Task> btasks;   // plan order (longest first)
   std::vector<bs::Bf16Pair> bpairs;
+  std::vector<bs::Bf16Cta> bctas;     // one per CTA: its slices of bstasks and bstages
+  std::vector<bs::Bf16Task> bstasks;  // tasks in execution order, CTA after CTA
+  std::vector<bs::Bf16Stage> bstages; // K stages in execution order, CTA after CTA
   std::vector<bs::MapDesc> maps;
   std::vector<unsigned char> map_bytes;   // encoded maps (128 bytes each)
   const void *maps_a_ptr = nullptr, *maps_b_ptr = nullptr;
@@ -95,10 +97,9 @@ struct bs_plan {
   size_t counter_bytes = 256;
   bs::PackCopy *d_pack = nullptr;
   bs::ZeroBlock *d_zero = nullptr;
-  bs::Bf16Task *d_btasks = nullptr;
-  int32_t *d_bcta_ptr = nullptr;
-  int32_t *d_bcta_items = nullptr;
-  bs::Bf16Pair *d_bpairs = nullptr;
+  bs::Bf16Cta *d_bctas = nullptr;
+  bs::Bf16Task *d_bstasks = nullptr;
+  bs::Bf16Stage *d_bstages = nullptr;
   void *d_maps = nullptr;
   void *d_ws_a = nullptr, *d_ws_b = nullptr;
   uint32_t *d_counter = nullptr;
