@@ -258,6 +258,7 @@ bs_status upload(bs_plan *P) {
   size_t o_rsegs = append_bytes(buf, P->gs.rsegs);
   size_t o_ksegs = append_bytes(buf, P->gs.ksegs);
   size_t o_tail = append_bytes(buf, P->ts.tail_elems);
+  size_t o_tdesc = append_bytes(buf, P->ts.tdesc);
   size_t o_tqp = append_bytes(buf, P->ts.tq_ptr);
   size_t o_tqi = append_bytes(buf, P->ts.tq_items);
   size_t o_pack = append_bytes(buf, P->pack_copies);
@@ -278,6 +279,7 @@ bs_status upload(bs_plan *P) {
   P->d_rsegs = (RowSeg *)(b + o_rsegs);
   P->d_ksegs = (KSeg *)(b + o_ksegs);
   P->d_tail = (int32_t *)(b + o_tail);
+  P->d_tdesc = (TailDesc *)(b + o_tdesc);
   P->d_tq_ptr = (int32_t *)(b + o_tqp);
   P->d_tq_items = (int32_t *)(b + o_tqi);
   P->d_pack = (PackCopy *)(b + o_pack);
@@ -691,6 +693,7 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
     p.rsegs = P->d_rsegs;
     p.ksegs = P->d_ksegs;
     p.tail_elems = (const int2 *)P->d_tail;
+    p.tdesc = P->d_tdesc;
     p.ntasks = (int32_t)P->ts.tasks.size();
     p.ntail = (int32_t)(P->ts.tail_elems.size() / 2);
     p.nct = (int32_t)((p.ntail + kThreads - 1) / kThreads);

@@ -135,21 +135,20 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
   const int e = w * 32 + lane;
   const bool ok = e < p.ntail;
   const int2 el = ok ? p.tail_elems[e] : make_int2(p.tail_elems[w * 32].x, 0);
-  const Group G = p.groups[el.x];
   const int r = el.y >> 16, c = el.y & 0xFFFF;
-  const int kg = ok ? G.k : 0;
-  const int kmax = __reduce_max_sync(0xFFFFFFFFu, (unsigned)kg);
-  const RowSeg *rs = p.rsegs + G.rseg_begin;
-  const KSeg *ks = p.ksegs + G.kseg_begin;
-  const RowSeg s = rs[find_rseg(rs, G.rseg_count, r)];
-  const int64_t lr = r - s.r0;
-  const int64_t ra = s.ra + lr * s.lda, rl = s.rl ? lr : 0;
-  KSeg k = ks[0];
-  const double *ap = p.A + ra + k.ka + rl * k.kl;
-  const double *bp = p.B + k.kb + c;
-  int64_t ldb = k.ldb;
+  // single-segment groups: addressing resolved at plan time, one table load
+  const TailDesc D = p.tdesc[el.x];
   double acc = 0.0;
-  if (__all_sync(0xFFFFFFFFu, G.kseg_count == 1)) {
+  int64_t cofs;
+  int flags;
+  if (__all_sync(0xFFFFFFFFu, D.k > 0)) {
+    const int kg = ok ? D.k : 0;
+    const int kmax = __reduce_max_sync(0xFFFFFFFFu, (unsigned)kg);
+    const double *ap = p.A + D.a0 + (int64_t)r * D.as;
+    const double *bp = p.B + D.b0 + c;
+    const int64_t ldb = D.ldb;
+    cofs = D.c0 + (int64_t)r * D.ldc + c;
+    flags = D.flags;
     // eight independent chains with their loads issued ahead, so that a warp
     // left alone on its SM at the end of the launch still keeps enough B rows
     // in flight to feed the FP64 pipe; steps past this lane's K load nothing
@@ -173,6 +172,21 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
       if (it < kg) a[0] = fma(__ldg(ap + it), __ldg(bp + it * ldb), a[0]);
     acc = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
   } else {
+    // general path: walk the group's row and inner segments
+    const Group G = p.groups[el.x];
+    const int kg = ok ? G.k : 0;
+    const int kmax = __reduce_max_sync(0xFFFFFFFFu, (unsigned)kg);
+    const RowSeg *rs = p.rsegs + G.rseg_begin;
+    const KSeg *ks = p.ksegs + G.kseg_begin;
+    const RowSeg s = rs[find_rseg(rs, G.rseg_count, r)];
+    const int64_t lr = r - s.r0;
+    const int64_t ra = s.ra + lr * s.lda, rl = s.rl ? lr : 0;
+    KSeg k = ks[0];
+    const double *ap = p.A + ra + k.ka + rl * k.kl;
+    const double *bp = p.B + k.kb + c;
+    int64_t ldb = k.ldb;
+    cofs = s.rc + lr * s.ldc + c;
+    flags = G.flags;
     int si = 0, rem = k.klen;
     for (int it = 0; it < kmax; ++it) {
       if (it < kg) {
@@ -191,8 +205,8 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
     }
   }
   if (ok) {
-    double *d = p.C + s.rc + lr * s.ldc + c;
-    if (G.flags & GF_ATOMIC) atomicAdd(d, acc);
+    double *d = p.C + cofs;
+    if (flags & GF_ATOMIC) atomicAdd(d, acc);
     else *d = acc;
   }
 }
@@ -200,7 +214,7 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
 __global__ void __launch_bounds__(kThreads, 4) fp64_grouped_kernel(Fp64Params p) {
   __shared__ TileSmem sm;
   // tile tasks, one CTA each, longest first
-  for (;;) {
+  for (; p.ntasks > 0;) {
     if (threadIdx.x == 0) sm.task = (int)atomicAdd(&p.counter[0], 1u);
     __syncthreads();
     const int t = sm.task;

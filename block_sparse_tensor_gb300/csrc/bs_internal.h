@@ -55,6 +55,18 @@ struct Group {
   int32_t kseg_begin, kseg_count;
 };
 
+// A tail group with one row segment and one inner segment, resolved at plan
+// time: output (r, c) is sum over kk < k of A[a0 + r*as + kk] * B[b0 + kk*ldb + c],
+// stored at C[c0 + r*ldc + c].  k = 0 marks a group that takes the general path
+// (several segments).
+struct TailDesc {
+  int64_t a0, as;
+  int64_t b0, ldb;
+  int64_t c0, ldc;
+  int32_t k;
+  int32_t flags;
+};
+
 enum TaskKind : int32_t { TK_TILE = 0 };
 
 // TK_TILE: one CTA computes rows m0 .. m0+tm-1, columns n0 .. n0+tn-1 of group `g`.
@@ -115,6 +127,7 @@ struct Fp64Params {
   const RowSeg *rsegs;
   const KSeg *ksegs;
   const int2 *tail_elems;
+  const TailDesc *tdesc;   // per group (used for tail groups)
   const int32_t *tq_ptr;    // per-SM queues of tail tasks: queue q holds tq_items[tq_ptr[q] .. tq_ptr[q+1])
   const int32_t *tq_items;  // tail task t covers tail_elems[kThreads t .. kThreads t + kThreads - 1]
   int32_t ntasks;

@@ -71,6 +71,7 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   const size_t n_rsegs = P->gs.rsegs.size() * sizeof(RowSeg);
   const size_t n_ksegs = P->gs.ksegs.size() * sizeof(KSeg);
   const size_t n_tail = P->ts.tail_elems.size() * sizeof(int32_t);
+  const size_t n_tdesc = P->ts.tdesc.size() * sizeof(TailDesc);
   const size_t n_tqp = P->ts.tq_ptr.size() * sizeof(int32_t);
   const size_t n_tqi = P->ts.tq_items.size() * sizeof(int32_t);
   const int nq = (int)std::max<size_t>(1, P->ts.tq_ptr.size()) - 1;
@@ -90,6 +91,8 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   off = align256(off + n_ksegs);
   const size_t o_tail = off;
   off = align256(off + n_tail);
+  const size_t o_tdesc = off;
+  off = align256(off + n_tdesc);
   const size_t o_tqp = off;
   off = align256(off + n_tqp);
   const size_t o_tqi = off;
@@ -120,7 +123,8 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   if (cudaMemsetAsync(b, 0, n_ctr, s) != cudaSuccess) return BS_ERR_CUDA;
   if (!up(o_tasks, P->ts.tasks.data(), n_tasks) || !up(o_groups, P->gs.groups.data(), n_groups) ||
       !up(o_rsegs, P->gs.rsegs.data(), n_rsegs) || !up(o_ksegs, P->gs.ksegs.data(), n_ksegs) ||
-      !up(o_tail, P->ts.tail_elems.data(), n_tail) || !up(o_tqp, P->ts.tq_ptr.data(), n_tqp) ||
+      !up(o_tail, P->ts.tail_elems.data(), n_tail) || !up(o_tdesc, P->ts.tdesc.data(), n_tdesc) ||
+      !up(o_tqp, P->ts.tq_ptr.data(), n_tqp) ||
       !up(o_tqi, P->ts.tq_items.data(), n_tqi) || !up(o_pack, P->pack_copies.data(), n_pack) ||
       !up(o_zero, P->zero_blocks.data(), n_zero))
     return BS_ERR_CUDA;
@@ -153,6 +157,7 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   p.rsegs = (const RowSeg *)(b + o_rsegs);
   p.ksegs = (const KSeg *)(b + o_ksegs);
   p.tail_elems = (const int2 *)(b + o_tail);
+  p.tdesc = (const TailDesc *)(b + o_tdesc);
   p.ntasks = (int32_t)P->ts.tasks.size();
   p.ntail = (int32_t)ntail;
   p.nct = (int32_t)((ntail + kThreads - 1) / kThreads);

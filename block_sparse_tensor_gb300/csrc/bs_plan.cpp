@@ -308,6 +308,7 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
   ts->tail_elems.clear();
   ts->tq_ptr.clear();
   ts->tq_items.clear();
+  ts->tdesc.assign(gs.groups.size(), TailDesc{});
   std::vector<std::pair<double, Task>> costed;
   std::vector<int32_t> tails;
   double exec = 0, work = 0;
@@ -345,6 +346,19 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
   std::vector<int32_t> elem_k;
   for (int32_t g : tails) {
     const Group &G = gs.groups[g];
+    if (G.rseg_count == 1 && G.kseg_count == 1) {   // resolve the addressing once, here
+      const RowSeg &rs = gs.rsegs[G.rseg_begin];
+      const KSeg &ks = gs.ksegs[G.kseg_begin];
+      TailDesc &d = ts->tdesc[g];
+      d.a0 = rs.ra + ks.ka;
+      d.as = rs.lda + (rs.rl ? ks.kl : 0);
+      d.b0 = ks.kb;
+      d.ldb = ks.ldb;
+      d.c0 = rs.rc;
+      d.ldc = rs.ldc;
+      d.k = G.k;
+      d.flags = G.flags;
+    }
     for (int32_t r = 0; r < G.m; ++r)
       for (int32_t c = 0; c < G.n; ++c) {
         ts->tail_elems.push_back(g);

@@ -21,6 +21,7 @@ struct GroupSet {
 struct TileSet {
   std::vector<Task> tasks;
   std::vector<int32_t> tail_elems;   // pairs: group, r << 16 | c
+  std::vector<TailDesc> tdesc;       // per group: resolved addressing of single-segment tail groups
   std::vector<int32_t> tq_ptr;       // per-SM queues of tail warp-tasks (LPT-balanced)
   std::vector<int32_t> tq_items;
   double executed_flops = 0;
@@ -92,6 +93,7 @@ struct bs_plan {
   bs::RowSeg *d_rsegs = nullptr;
   bs::KSeg *d_ksegs = nullptr;
   int32_t *d_tail = nullptr;
+  bs::TailDesc *d_tdesc = nullptr;
   int32_t *d_tq_ptr = nullptr;
   int32_t *d_tq_items = nullptr;
   size_t counter_bytes = 256;
