@@ -21,17 +21,20 @@ LIB_PATH = os.path.join(_HERE, "libbs.so")
 
 F64, BF16_F32 = 0, 1
 AXIS_AUTO, AXIS_CONTRACTION, AXIS_FREE, AXIS_NONE = 0, 1, 2, 3
+DEBUG_WITHHOLD_COPY, DEBUG_MERGE_UNCHECKED = 1, 2
+ERR_HOLE = 10
 PACK_AUTO, PACK_NEVER, PACK_ALWAYS = 0, 1, 2
 LAYOUT_FLAGS = {"blockrow": 0, "rowpanel": 1, "colpanel": 2, "charge_sorted": 4, "align16": 8}
 STATUS = {0: "ok", 1: "invalid argument", 2: "shape mismatch", 3: "unsupported", 4: "out of memory",
           5: "CUDA error", 6: "device wait timed out", 7: "misaligned", 8: "device check failed",
-          9: "size overflow"}
+          9: "size overflow", 10: "group is not a hole-free view of its blocks"}
 
 EXPORTED = ["bs_layout_create", "bs_layout_query", "bs_layout_blocks", "bs_layout_destroy",
             "bs_plan_options_default", "bs_plan_create", "bs_plan_c_layout", "bs_plan_stats_get",
             "bs_plan_groups", "bs_plan_triples", "bs_contract", "bs_contract_host",
             "bs_contract_uncoalesced", "bs_plan_last_device_error", "bs_plan_destroy",
-            "bs_status_string", "bs_version", "bs_calibrate", "bs_contract_noalloc"]
+            "bs_status_string", "bs_version", "bs_calibrate", "bs_contract_noalloc",
+            "bs_plan_check_groups"]
 
 
 class BsError(RuntimeError):
@@ -107,6 +110,7 @@ def _load(path: str = LIB_PATH):
         "bs_version": (ctypes.c_char_p, []),
         "bs_calibrate": (st, [P, P]),
         "bs_contract_noalloc": (st, [P, P, P, P, P]),
+        "bs_plan_check_groups": (st, [P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -258,6 +262,12 @@ class Plan:
         out = np.zeros((max(n.value, 1), 8), np.int64)
         _check(lib.bs_plan_groups(self.h, ctypes.byref(n), out.ctypes.data), "bs_plan_groups")
         return out[:n.value]
+
+    def check_groups(self):
+        """(status, first failing group or -1) of bs_plan_check_groups."""
+        bad = ctypes.c_int64()
+        status = lib.bs_plan_check_groups(self.h, ctypes.byref(bad))
+        return status, bad.value
 
     def triples(self):
         """(group_ptr, triples) with triples an (n, 3) int32 array of (i, k, j)."""

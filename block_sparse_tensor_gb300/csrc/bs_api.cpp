@@ -337,6 +337,7 @@ const char *bs_status_string(bs_status s) {
     case BS_ERR_MISALIGNED: return "misaligned buffer or view";
     case BS_ERR_DEVICE: return "device-side check failed";
     case BS_ERR_OVERFLOW: return "size overflow";
+    case BS_ERR_HOLE: return "group is not a hole-free view of its blocks";
   }
   return "unknown status";
 }
@@ -410,6 +411,9 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
   if (!A->cols.same_as(B->rows)) return BS_ERR_SHAPE_MISMATCH;
   if (dtype == BS_BF16_F32 && (o.axis_policy == BS_AXIS_FREE || o.axis_policy == BS_AXIS_NONE))
     return BS_ERR_UNSUPPORTED;
+  // groups with holes are for testing the validator only: such a plan never runs
+  const bool unchecked = (o.debug_flags & BS_DEBUG_MERGE_UNCHECKED) != 0;
+  if (unchecked && !o.host_only) return BS_ERR_INVALID_ARG;
   const auto t0 = std::chrono::steady_clock::now();
   bs_plan *P = new (std::nothrow) bs_plan();
   if (!P) return BS_ERR_OOM;
@@ -488,7 +492,7 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
             }
           }
           const auto tg0 = std::chrono::steady_clock::now();
-          GroupSet gs = ax == BS_AXIS_CONTRACTION ? make_contraction_groups(*Ae, *Be, P->C, o.merge_rows != 0, false)
+          GroupSet gs = ax == BS_AXIS_CONTRACTION ? make_contraction_groups(*Ae, *Be, P->C, o.merge_rows != 0, false, unchecked)
                         : ax == BS_AXIS_FREE      ? make_free_groups(*Ae, *Be, P->C)
                                                   : make_triple_groups(*Ae, *Be, P->C);
           const auto tg1 = std::chrono::steady_clock::now();
@@ -529,7 +533,7 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
       (void)best_pack;
     } else {
       // BF16: contraction axis; views must satisfy the tensor-map rules, else gather
-      GroupSet gs = make_contraction_groups(P->A, P->B, P->C, o.merge_rows != 0, false);
+      GroupSet gs = make_contraction_groups(P->A, P->B, P->C, o.merge_rows != 0, false, unchecked);
       bool need_pack = !groups_tma_ok(gs) || o.pack_policy == BS_PACK_ALWAYS;
       if (need_pack && o.pack_policy == BS_PACK_NEVER) {
         delete P;
@@ -543,7 +547,7 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
           return st;
         }
         P->pack_a = P->pack_b = true;
-        gs = make_contraction_groups(P->A_pk, P->B_pk, P->C, o.merge_rows != 0, false);
+        gs = make_contraction_groups(P->A_pk, P->B_pk, P->C, o.merge_rows != 0, false, unchecked);
       }
       P->gs = std::move(gs);
       P->axis = BS_AXIS_CONTRACTION;
@@ -656,6 +660,108 @@ bs_status bs_plan_triples(const bs_plan *P, int64_t *ntriples, int64_t *ngroups,
   *ngroups = (int64_t)P->gs.groups.size();
   if (group_ptr) std::memcpy(group_ptr, tp.data(), tp.size() * sizeof(int64_t));
   if (out && !tr.empty()) std::memcpy(out, tr.data(), tr.size() * sizeof(int32_t));
+  return BS_OK;
+}
+
+bs_status bs_plan_check_groups(const bs_plan *P, int64_t *bad_group) {
+  if (!P) return BS_ERR_INVALID_ARG;
+  if (bad_group) *bad_group = -1;
+  // the layouts the kernels read
+  const bs_layout &A = P->pack_a ? P->A_pk : P->A;
+  const bs_layout &B = P->pack_b ? P->B_pk : P->B;
+  const bs_layout &C = P->C;
+  std::vector<int64_t> tp;
+  std::vector<int32_t> tr;
+  group_triples(P->gs, &tp, &tr);
+  std::vector<int32_t> rows, ks;
+  std::vector<int64_t> roff, koff;
+  for (size_t g = 0; g < P->gs.groups.size(); ++g) {
+    const Group &G = P->gs.groups[g];
+    bool ok = tp[g + 1] > tp[g];
+    // row sectors and inner sectors in order of first appearance, with offsets
+    rows.clear();
+    ks.clear();
+    int32_t jcol = ok ? tr[3 * tp[g] + 2] : -1;
+    for (int64_t t = tp[g]; ok && t < tp[g + 1]; ++t) {
+      const int32_t i = tr[3 * t], k = tr[3 * t + 1], j = tr[3 * t + 2];
+      ok = j == jcol;
+      if (std::find(rows.begin(), rows.end(), i) == rows.end()) rows.push_back(i);
+      if (std::find(ks.begin(), ks.end(), k) == ks.end()) ks.push_back(k);
+    }
+    int64_t msum = 0, ksum = 0;
+    roff.assign(rows.size(), 0);
+    koff.assign(ks.size(), 0);
+    for (size_t a = 0; a < rows.size(); ++a) {
+      roff[a] = msum;
+      msum += A.rows.d[rows[a]];
+    }
+    for (size_t b = 0; b < ks.size(); ++b) {
+      koff[b] = ksum;
+      ksum += A.cols.d[ks[b]];
+    }
+    // (1) the triples tile the M x K rectangle: every pair, once
+    ok = ok && msum == G.m && ksum == G.k && B.cols.d[jcol] == G.n &&
+         tp[g + 1] - tp[g] == (int64_t)rows.size() * (int64_t)ks.size();
+    if (ok) {
+      std::vector<char> seen(rows.size() * ks.size(), 0);
+      for (int64_t t = tp[g]; ok && t < tp[g + 1]; ++t) {
+        const size_t a = std::find(rows.begin(), rows.end(), tr[3 * t]) - rows.begin();
+        const size_t b = std::find(ks.begin(), ks.end(), tr[3 * t + 1]) - ks.begin();
+        ok = !seen[a * ks.size() + b];
+        seen[a * ks.size() + b] = 1;
+      }
+    }
+    // (2) the views address every block where its layout stores it
+    const RowSeg *rs = P->gs.rsegs.data() + G.rseg_begin;
+    const KSeg *kg = P->gs.ksegs.data() + G.kseg_begin;
+    auto rseg_of = [&](int64_t r) -> const RowSeg * {
+      for (int32_t q = 0; q < G.rseg_count; ++q)
+        if (r >= rs[q].r0 && r < rs[q].r0 + rs[q].rows) return rs + q;
+      return nullptr;
+    };
+    auto kseg_of = [&](int64_t kk) -> const KSeg * {
+      for (int32_t q = 0; q < G.kseg_count; ++q)
+        if (kk >= kg[q].k0 && kk < kg[q].k0 + kg[q].klen) return kg + q;
+      return nullptr;
+    };
+    // A(r, kk) = A[RA + KA + RL * KL], B(kk, c) = B[KB + c], C(r, c) = C[RC + c]
+    auto a_addr = [&](int64_t r, int64_t kk, int64_t *out) {
+      const RowSeg *s = rseg_of(r);
+      const KSeg *q = kseg_of(kk);
+      if (!s || !q) return false;
+      const int64_t lr = r - s->r0;
+      *out = s->ra + lr * s->lda + q->ka + (kk - q->k0) + (s->rl ? lr : 0) * q->kl;
+      return true;
+    };
+    for (int64_t t = tp[g]; ok && t < tp[g + 1]; ++t) {
+      const int32_t i = tr[3 * t], k = tr[3 * t + 1];
+      const int64_t r = roff[std::find(rows.begin(), rows.end(), i) - rows.begin()];
+      const int64_t kk = koff[std::find(ks.begin(), ks.end(), k) - ks.begin()];
+      const int32_t ba = A.find(i, k), bb = B.find(k, jcol), bc = C.find(i, jcol);
+      if (ba < 0 || bb < 0 || bc < 0) {
+        ok = false;
+        break;
+      }
+      const bs_block_info &ia = A.blocks[ba], &ib = B.blocks[bb], &ic = C.blocks[bc];
+      int64_t x0 = 0, x1 = 0;
+      ok = a_addr(r, kk, &x0) && x0 == ia.offset;
+      if (ok && ia.rows > 1) ok = a_addr(r + 1, kk, &x1) && x1 - x0 == ia.ld;
+      if (ok && ia.cols > 1) ok = a_addr(r, kk + ia.cols - 1, &x1) && x1 - x0 == ia.cols - 1;
+      const KSeg *q = kseg_of(kk);
+      ok = ok && q && q->kb + (kk - q->k0) * q->ldb == ib.offset && (ib.rows == 1 || q->ldb == ib.ld);
+      if (ok && ib.rows > 1) {
+        const KSeg *q2 = kseg_of(kk + ib.rows - 1);
+        ok = q2 == q;
+      }
+      const RowSeg *s = rseg_of(r);
+      ok = ok && s && s->rc + (r - s->r0) * s->ldc == ic.offset && (ic.rows == 1 || s->ldc == ic.ld);
+      if (ok && ic.rows > 1) ok = rseg_of(r + ic.rows - 1) == s;
+    }
+    if (!ok) {
+      if (bad_group) *bad_group = (int64_t)g;
+      return BS_ERR_HOLE;
+    }
+  }
   return BS_OK;
 }
 

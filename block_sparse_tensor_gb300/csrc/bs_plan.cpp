@@ -48,7 +48,7 @@ struct Entry {
 // One group per C block: the inner blocks in A's storage order, merged into
 // runs where both the A view and the B view continue with the same stride.
 GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C, bool merge_rows,
-                                 bool atomic) {
+                                 bool atomic, bool unchecked) {
   Builder bd;
   GroupSet &gs = bd.gs;
   gs.tptr.push_back(0);
@@ -85,8 +85,9 @@ GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const b
           const auto &a0 = A.blocks[last_entries[j][e].blk_a];
           const auto &a1 = A.blocks[ent[e].blk_a];
           // same inner block, same B block, A rows continuing the group's rows
-          ok = last_entries[j][e].k == ent[e].k && last_entries[j][e].blk_b == ent[e].blk_b && a1.ld == a0.ld &&
-               a1.offset == a0.offset + (int64_t)g.m * a0.ld;
+          // (`unchecked`, a testing switch, skips the first two conditions)
+          ok = (unchecked || (last_entries[j][e].k == ent[e].k && last_entries[j][e].blk_b == ent[e].blk_b)) &&
+               a1.ld == a0.ld && a1.offset == a0.offset + (int64_t)g.m * a0.ld;
         }
         if (ok) {
           // last_entries keeps the group's first row sector, which the offsets are relative to

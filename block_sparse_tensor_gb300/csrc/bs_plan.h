@@ -40,7 +40,7 @@ struct PlanModel {
 };
 
 GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C, bool merge_rows,
-                                 bool atomic);
+                                 bool atomic, bool unchecked = false);
 GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C);
 GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C);
 void group_triples(const GroupSet &gs, std::vector<int64_t> *ptr, std::vector<int32_t> *out);

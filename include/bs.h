@@ -47,7 +47,8 @@ typedef enum bs_status {
   BS_ERR_TIMEOUT = 6,         /* a bounded device-side wait ran out (reported by the kernel) */
   BS_ERR_MISALIGNED = 7,      /* a buffer or view breaks the 16-byte rule of the chosen path */
   BS_ERR_DEVICE = 8,          /* a device-side consistency check failed */
-  BS_ERR_OVERFLOW = 9         /* an element count or offset does not fit in int64 / int32 */
+  BS_ERR_OVERFLOW = 9,        /* an element count or offset does not fit in int64 / int32 */
+  BS_ERR_HOLE = 10            /* a coalesced group is not a hole-free view of its blocks */
 } bs_status;
 
 /* One sector axis: n sectors, each with a U(1) charge, an optional Z2 parity
@@ -151,13 +152,16 @@ typedef struct bs_plan_options {
   double fp64_gflops;         /* sustained FP64 pipe rate of the grouped kernel */
   double atomic_penalty;      /* relative cost of an atomic scatter store vs a plain store */
   int32_t wait_timeout_ms;    /* limit of every device-side wait (BF16 path); <= 0: 2000 ms */
-  int32_t debug_flags;        /* testing only: BS_DEBUG_WITHHOLD_COPY makes the BF16 producer
-                                 skip its first copy so the consumer's bounded wait runs out
-                                 and the kernel reports BS_ERR_TIMEOUT; 0 in normal use */
+  int32_t debug_flags;        /* testing only, 0 in normal use: BS_DEBUG_WITHHOLD_COPY makes
+                                 the BF16 producer skip its first copy so the consumer's bounded
+                                 wait runs out and the kernel reports BS_ERR_TIMEOUT;
+                                 BS_DEBUG_MERGE_UNCHECKED lets merge_rows stack row sectors
+                                 whose inner blocks differ (groups with holes, for testing
+                                 bs_plan_check_groups); such a plan must be host_only */
   int32_t reserved[6];
 } bs_plan_options;
 
-enum { BS_DEBUG_WITHHOLD_COPY = 1 };
+enum { BS_DEBUG_WITHHOLD_COPY = 1, BS_DEBUG_MERGE_UNCHECKED = 2 };
 
 void bs_plan_options_default(bs_plan_options *opts);
 
@@ -212,6 +216,20 @@ bs_status bs_plan_groups(const bs_plan *plan, int64_t *ngroups, int64_t *out);
  * delimit group g.  Pass NULL arrays to get the sizes. */
 bs_status bs_plan_triples(const bs_plan *plan, int64_t *ntriples, int64_t *ngroups, int64_t *group_ptr,
                           int32_t *out);
+
+/* Proof that every group is a hole-free view of its blocks (uni20 design note
+ * "block coalescing", "Why single-axis coalescing is hole-free", and its
+ * LocalSpace keys stacked as a second coalesced axis).  For each group, with
+ * the row sectors and inner sectors of its triples taken in order of first
+ * appearance: (1) the triples are exactly every (row sector, inner sector)
+ * pair, once each, and the sectors' dimensions add up to the group's M and K
+ * (and the column sector's to N), so the blocks tile the M x K rectangle with
+ * no hole; (2) the group's row and inner segments address each triple's A, B
+ * and C blocks exactly where the operand layouts (after any gather) store them:
+ * first element and leading dimension.  Host only, reads no device memory.
+ * Returns BS_OK, or BS_ERR_HOLE with the first failing group in *bad_group
+ * (may be NULL); -1 there when every group passes. */
+bs_status bs_plan_check_groups(const bs_plan *plan, int64_t *bad_group);
 
 /* Enqueue C = A B on `stream` and return at once.  A, B, C are device
  * pointers to buffers laid out per the plan's A, B and C layouts; every

@@ -118,6 +118,8 @@ def test_plan_covers_each_triple_once_and_is_hole_free(cfg, pol, lay):
             assert len(t) == 1
     flops = sum(2 * int(w.rows.d[i]) * int(w.inner.d[k]) * int(w.cols.d[j]) for (i, k, j) in want)
     assert st["useful_flops"] == pytest.approx(flops, rel=1e-12)
+    # the library's own proof: blocks tile every group and sit where its views point
+    assert P.check_groups() == (0, -1)
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 4])
@@ -142,6 +144,53 @@ def test_localspace_keys_merge_into_taller_groups():
     assert np.all(g[:, 1] % 4 == 0)
     P2, _, _ = host_plan(w, merge_rows=0)
     assert len(P2.groups()) == 652
+    # two-axis groups (four key rows x several inner sectors), each proved hole-free
+    ptr, tr = P.triples()
+    two_axis = sum(1 for g0, g1 in zip(ptr[:-1], ptr[1:])
+                   if len(set(tr[g0:g1, 0])) == 4 and len(set(tr[g0:g1, 1])) > 1)
+    assert two_axis > 100
+    assert P.check_groups() == (0, -1)
+    assert P2.check_groups() == (0, -1)
+    P3, _, _ = host_plan(w, pack_policy=bs.PACK_ALWAYS, la="blockrow", lb="blockrow")
+    assert P3.check_groups() == (0, -1)
+
+
+def _two_row_problem():
+    """Two row sectors (charges 0 and 1) of equal dimension whose inner blocks
+    differ (charges -1..1 and 0..2) but have the same count and panel width."""
+    rows = bsgen.Axis(np.array([0, 1]), np.array([2, 2]))
+    inner = bsgen.Axis(np.array([-1, 0, 1, 2]), np.array([3, 3, 3, 3]))
+    cols = bsgen.Axis(np.array([0]), np.array([2]))
+    A = bs.Layout(rows, inner, bsgen.Rule(-1, 1), "rowpanel|charge_sorted", 8)
+    B = bs.Layout(inner, cols, bsgen.Rule(-10, 10), "colpanel|charge_sorted", 8)
+    return A, B
+
+
+def test_group_validator_finds_a_planted_hole():
+    """With the same-inner-blocks check switched off, row stacking puts both rows
+    into one group whose 2 x 4 rectangle holds only 6 of its 8 blocks: the
+    validator must report that group.  With the check on, the rows stay apart."""
+    A, B = _two_row_problem()
+    ok = bs.Plan(A, B, bs.F64, host_only=1, merge_rows=1, axis_policy=bs.AXIS_CONTRACTION, c_layout_flags="rowpanel")
+    assert len(ok.groups()) == 2
+    assert ok.check_groups() == (0, -1)
+    bad = bs.Plan(A, B, bs.F64, host_only=1, merge_rows=1, axis_policy=bs.AXIS_CONTRACTION, c_layout_flags="rowpanel",
+                  debug_flags=bs.DEBUG_MERGE_UNCHECKED)
+    assert len(bad.groups()) == 1
+    assert bad.check_groups() == (bs.ERR_HOLE, 0)
+
+
+def test_unchecked_merge_is_refused_for_a_device_plan():
+    A, B = _two_row_problem()
+    with pytest.raises(bs.BsError) as e:
+        bs.Plan(A, B, bs.F64, merge_rows=1, debug_flags=bs.DEBUG_MERGE_UNCHECKED)
+    assert e.value.code == 1
+
+
+def test_group_validator_on_the_stress_workload():
+    w = bsgen.config5()
+    P, _, _ = host_plan(w)
+    assert P.check_groups() == (0, -1)
 
 
 def test_band_layouts_give_single_view_groups():
