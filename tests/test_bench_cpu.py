@@ -24,8 +24,8 @@ def _json_lines(out: str):
 
 
 def test_reference_arm_prints_one_line():
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3"],
-                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3",
+                        "--cpu-workers", "2"], cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
@@ -33,13 +33,14 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["unit"] == "GFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["warmup"] >= 3 and d["steps"] == 2
+    assert d["cpu_baseline"]["cores"] == 2
 
 
 def test_reference_arm_under_torchrun_two_ranks():
     port = _free_port()
     r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
                         "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
-                        "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                        "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-workers", "2"],
                        cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)
@@ -73,3 +74,19 @@ def test_max_over_ranks_with_gloo_world_size_two():
     for p, (o, e) in zip(procs, outs):
         assert p.returncode == 0, e[-2000:]
         assert o.strip().startswith("ok")
+
+
+def test_oracle_pool_covers_every_c_block_once():
+    """The all-cores baseline deals each populated C block to exactly one worker."""
+    import numpy as np
+    import bench
+    import oracle
+    pool = bench.OraclePool(1, workers=3)
+    try:
+        got = np.concatenate(pool.parts)
+        want = np.argwhere(oracle.problem(bench.bsgen.get(1)).mc)
+        assert len(got) == len(want) == len({tuple(x) for x in got.tolist()})
+        assert {tuple(x) for x in got.tolist()} == {tuple(x) for x in want.tolist()}
+        pool.step()
+    finally:
+        pool.close()
