@@ -329,7 +329,26 @@ def per_config(bs, torch, flush, stream, calib, peaks, args, clock_mhz):
         torch.cuda.empty_cache()
     out["chain"] = chain_record(bs, torch, flush, stream)
     log(f"[bench] chain: {json.dumps(out['chain'])}")
+    out["bucket"] = bucket_record(bs, torch, flush, stream)
+    log(f"[bench] bucket: {json.dumps(out['bucket'])}")
     return out
+
+
+def bucket_record(bs, torch, flush, stream):
+    """Exact grouping against tail groups padded to power-of-two buckets, workload 2."""
+    w = bsgen.config2()
+    rec = {"workload": w.name}
+    for name, axis in (("contraction", bs.AXIS_CONTRACTION), ("none", bs.AXIS_NONE)):
+        for pad in (0, 1):
+            pb = Problem(bs, torch, w, axis_policy=axis, bucket_pad=pad)
+            ms = statistics.median(time_steps(torch, lambda: bs.contract(pb.P, pb.a, pb.b, pb.c, stream), 50, 3, flush,
+                                              stream))
+            st = pb.stats
+            rec[f"{name}_{'padded' if pad else 'exact'}"] = {
+                "ms": ms, "gflops": st["useful_flops"] / (ms * 1e-3) / 1e9,
+                "executed_over_useful": st["executed_flops"] / st["useful_flops"], "tail_pieces": st["tail_tasks"]}
+            del pb
+    return rec
 
 
 def chain_record(bs, torch, flush, stream):

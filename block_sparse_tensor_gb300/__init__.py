@@ -65,7 +65,7 @@ class PlanOptions(ctypes.Structure):
                 ("t_segment_us", ctypes.c_double), ("pack_gbs", ctypes.c_double),
                 ("fp64_gflops", ctypes.c_double), ("atomic_penalty", ctypes.c_double),
                 ("wait_timeout_ms", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 6)]
+                ("bucket_pad", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
 
 
 class PlanStats(ctypes.Structure):

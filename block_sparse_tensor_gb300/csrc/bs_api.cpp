@@ -435,6 +435,11 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
     if (o.pack_gbs > 0) pm.pack_gbs = o.pack_gbs;
     if (o.fp64_gflops > 0) pm.fp64_gflops = o.fp64_gflops;
     if (o.atomic_penalty > 0) pm.atomic_penalty = o.atomic_penalty;
+    if (o.bucket_pad < 0 || o.bucket_pad > 1) {
+      delete P;
+      return BS_ERR_INVALID_ARG;
+    }
+    pm.bucket_pad = o.bucket_pad == 1;
     if (!o.host_only) {
       int dev = 0, major = 0, minor = 0;
       if (cudaGetDevice(&dev) != cudaSuccess) {

@@ -141,9 +141,11 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
   double acc = 0.0;
   int64_t cofs;
   int flags;
+  bool live = ok;   // this lane owns a real output (padded lanes of a bucket do not)
   if (__all_sync(0xFFFFFFFFu, D.k > 0)) {
-    const int kg = ok ? D.k : 0;
-    const int kmax = __reduce_max_sync(0xFFFFFFFFu, (unsigned)kg);
+    live = ok && r < D.m && c < D.n;
+    const int kg = live ? D.k : 0;   // steps that load data
+    const int kmax = __reduce_max_sync(0xFFFFFFFFu, ok ? (unsigned)D.kpad : 0u);   // steps run
     const double *ap = p.A + D.a0 + (int64_t)r * D.as;
     const double *bp = p.B + D.b0 + c;
     const int64_t ldb = D.ldb;
@@ -204,7 +206,7 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
       }
     }
   }
-  if (ok) {
+  if (live) {
     double *d = p.C + cofs;
     if (flags & GF_ATOMIC) atomicAdd(d, acc);
     else *d = acc;

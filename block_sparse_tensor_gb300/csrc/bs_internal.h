@@ -58,13 +58,18 @@ struct Group {
 // A tail group with one row segment and one inner segment, resolved at plan
 // time: output (r, c) is sum over kk < k of A[a0 + r*as + kk] * B[b0 + kk*ldb + c],
 // stored at C[c0 + r*ldc + c].  k = 0 marks a group that takes the general path
-// (several segments).
+// (several segments).  When the plan pads the group to a bucket shape, its
+// outputs run kpad steps (loads past k give zero) and its list may carry
+// outputs with r >= m or c >= n that load and store nothing.
 struct TailDesc {
   int64_t a0, as;
   int64_t b0, ldb;
   int64_t c0, ldc;
   int32_t k;
   int32_t flags;
+  int32_t kpad;
+  int32_t m, n;
+  int32_t pad_;
 };
 
 enum TaskKind : int32_t { TK_TILE = 0 };

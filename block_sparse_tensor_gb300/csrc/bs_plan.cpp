@@ -341,12 +341,34 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
   }
   // Small groups: every output gets its own lane.  Groups are ordered by
   // decreasing K so that the 32 lanes of a warp run loops of nearly equal
-  // length; warps take 32 consecutive outputs at a time.
-  std::stable_sort(tails.begin(), tails.end(),
-                   [&](int32_t a, int32_t b) { return gs.groups[a].k > gs.groups[b].k; });
+  // length; warps take 32 consecutive outputs at a time.  With bucket_pad a
+  // single-segment group is padded to power-of-two M, N and K and groups of
+  // one padded shape are listed together: they run as one batched call whose
+  // padded lanes and steps add only zeros.
+  auto pow2 = [](int32_t x) {
+    int32_t p = 1;
+    while (p < x) p <<= 1;
+    return p;
+  };
+  auto padded = [&](int32_t g, int32_t *mp, int32_t *np, int32_t *kp) {
+    const Group &G = gs.groups[g];
+    const bool pad = pm.bucket_pad && G.rseg_count == 1 && G.kseg_count == 1;
+    *mp = pad ? pow2(G.m) : G.m;
+    *np = pad ? pow2(G.n) : G.n;
+    *kp = pad ? pow2(G.k) : G.k;
+  };
+  std::stable_sort(tails.begin(), tails.end(), [&](int32_t a, int32_t b) {
+    int32_t ma, na, ka, mb, nb, kb;
+    padded(a, &ma, &na, &ka);
+    padded(b, &mb, &nb, &kb);
+    if (!pm.bucket_pad) return ka > kb;   // exact: by K only, as listed
+    return std::make_tuple(-ka, ma, na) < std::make_tuple(-kb, mb, nb);
+  });
   std::vector<int32_t> elem_k;
   for (int32_t g : tails) {
     const Group &G = gs.groups[g];
+    int32_t mp, np, kp;
+    padded(g, &mp, &np, &kp);
     if (G.rseg_count == 1 && G.kseg_count == 1) {   // resolve the addressing once, here
       const RowSeg &rs = gs.rsegs[G.rseg_begin];
       const KSeg &ks = gs.ksegs[G.kseg_begin];
@@ -359,12 +381,15 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
       d.ldc = rs.ldc;
       d.k = G.k;
       d.flags = G.flags;
+      d.kpad = kp;
+      d.m = G.m;
+      d.n = G.n;
     }
-    for (int32_t r = 0; r < G.m; ++r)
-      for (int32_t c = 0; c < G.n; ++c) {
+    for (int32_t r = 0; r < mp; ++r)
+      for (int32_t c = 0; c < np; ++c) {
         ts->tail_elems.push_back(g);
         ts->tail_elems.push_back((r << 16) | c);
-        elem_k.push_back(G.k);
+        elem_k.push_back(kp);
       }
   }
   // Tail tasks of kThreads outputs (one CTA, one output per thread): the 8

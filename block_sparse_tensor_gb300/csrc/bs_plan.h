@@ -37,6 +37,7 @@ struct PlanModel {
   double task_slots = 4096;   // LPT weight of a task's fixed cost, in lane-flop units
   int parallel_ctas = 456;
   int sms = 152;
+  bool bucket_pad = false;    // pad single-segment tail groups to power-of-two shapes
 };
 
 GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C, bool merge_rows,

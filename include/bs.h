@@ -158,7 +158,12 @@ typedef struct bs_plan_options {
                                  BS_DEBUG_MERGE_UNCHECKED lets merge_rows stack row sectors
                                  whose inner blocks differ (groups with holes, for testing
                                  bs_plan_check_groups); such a plan must be host_only */
-  int32_t reserved[6];
+  int32_t bucket_pad;         /* FP64 tail: 0 (default) computes every small group exactly; 1 pads
+                                 each single-segment tail group to power-of-two M, N and K so that
+                                 groups of one padded shape run as one batched call (uni20 design
+                                 note "block coalescing", Open questions: bucketing near-same
+                                 shapes by padding); padded rows, columns and K add only zeros */
+  int32_t reserved[5];
 } bs_plan_options;
 
 enum { BS_DEBUG_WITHHOLD_COPY = 1, BS_DEBUG_MERGE_UNCHECKED = 2 };

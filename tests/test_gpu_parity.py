@@ -121,6 +121,24 @@ def test_integer_inputs_bit_exact(seed, pol):
     compare(r, r.run(), exact=True)
 
 
+@pytest.mark.parametrize("cfg", [1, 2])
+@pytest.mark.parametrize("pol", ["contraction", "none", "free"])
+def test_bucket_padding_matches_oracle(cfg, pol):
+    """Tail groups padded to power-of-two shapes (batched buckets): the padded lanes
+    and steps add only zeros, so every block still matches the oracle."""
+    r = Run(bsgen.get(cfg), bucket_pad=1, **POLICIES[pol])
+    assert r.P.stats()["executed_flops"] >= r.P.stats()["useful_flops"]
+    compare(r, r.run())
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_bucket_padding_integer_inputs_bit_exact(seed):
+    w = bsgen.tiny_random(100 + seed, values="int3", max_sectors=14, max_dim=9 if seed % 2 else 30)
+    r = Run(w, *LAYOUTS[["panels", "blockrow", "mixed"][seed % 3]], bucket_pad=1,
+            **POLICIES[["contraction", "none", "free", "auto"][seed % 4]])
+    compare(r, r.run(), exact=True)
+
+
 @pytest.mark.parametrize("seed", range(8))
 def test_bf16_integer_inputs_bit_exact(seed):
     """|x| <= 3 integers are exact in bfloat16 and every FP32 partial sum stays exact."""

@@ -283,3 +283,21 @@ def test_chain_stage2_plans_on_stage1_c_layout():
     assert s2["c_blocks"] == int(oracle.product_mask(pr1.mc, oracle.rule_mask(w2.inner, w2.cols, w2.rule_b)).sum())
     # T in charge-sorted row panels makes every stage-2 group one view
     assert np.all(P2.groups()[:, 5] == 1)
+
+
+def test_bucket_padding_accounts_its_waste():
+    """Power-of-two buckets: the same triples and groups, more executed flops (the
+    padding), and nothing changes when bucket_pad is off."""
+    w = bsgen.config2()
+    for axis in (bs.AXIS_CONTRACTION, bs.AXIS_NONE):
+        ex, _, _ = host_plan(w, axis_policy=axis)
+        bk, _, _ = host_plan(w, axis_policy=axis, bucket_pad=1)
+        se, sb = ex.stats(), bk.stats()
+        assert sb["triples"] == se["triples"] and sb["groups"] == se["groups"]
+        assert sb["useful_flops"] == se["useful_flops"]
+        assert se["executed_flops"] < 1.001 * se["useful_flops"]
+        assert sb["executed_flops"] > 1.5 * sb["useful_flops"]
+        assert sb["tail_tasks"] > se["tail_tasks"]
+        assert bk.check_groups() == (0, -1)
+    with pytest.raises(bs.BsError):
+        host_plan(w, bucket_pad=2)
