@@ -176,7 +176,7 @@ typedef struct bs_plan_stats {
   int64_t groups;             /* coalesced groups (one GEMM each) */
   int64_t tasks;              /* persistent-kernel work items */
   int64_t tile_tasks;         /* CTA-wide tiles */
-  int64_t tail_tasks;         /* warp bundles of tiny groups */
+  int64_t tail_tasks;         /* CTA-sized pieces (256 outputs, one per thread) of the small-group list */
   int64_t segments;           /* zero-copy view segments over all groups */
   int64_t packed_bytes;       /* bytes gathered per contraction (0: zero-copy) */
   int64_t workspace_bytes;    /* device workspace owned by the plan */
@@ -186,7 +186,7 @@ typedef struct bs_plan_stats {
   int32_t launches;           /* kernels one bs_contract enqueues */
   double useful_flops;        /* sum over triples of 2 * d_i * d_k * d_j */
   double useful_bytes;        /* populated A + B elements read once, C written once */
-  double executed_flops;      /* flops the kernels issue, tile padding included */
+  double executed_flops;      /* flops the kernels issue, idle lanes and bucket padding included */
   double model_us;            /* cost-model estimate of one contraction */
   double model_us_alt;        /* estimate for the other axis / pack choice */
   double plan_ms;             /* host time spent in bs_plan_create */
