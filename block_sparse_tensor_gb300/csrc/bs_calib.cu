@@ -46,7 +46,7 @@ __global__ void dfma_probe(double *out, double seed, int active) {
 
 __global__ void empty_kernel() {}
 
-__global__ void copy_probe(const double4 *src, double4 *dst, size_t n) {
+__global__ void copy_probe(const double4_32a *src, double4_32a *dst, size_t n) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
     dst[i] = src[i];
 }
@@ -96,9 +96,9 @@ extern "C" bs_status bs_calibrate(bs_calibration *out, void *stream) {
       st = BS_ERR_OOM;
       break;
     }
-    const size_t n4 = copy_bytes / sizeof(double4);
+    const size_t n4 = copy_bytes / sizeof(double4_32a);
     const double ms = timed([&] {
-      copy_probe<<<sms * 8, 256, 0, s>>>((const double4 *)bufs, (double4 *)((char *)bufs + copy_bytes), n4);
+      copy_probe<<<sms * 8, 256, 0, s>>>((const double4_32a *)bufs, (double4_32a *)((char *)bufs + copy_bytes), n4);
     }, 10);
     out->copy_gbs = 2.0 * copy_bytes / (ms * 1e6);
     out->sm_count = sms;
