@@ -247,10 +247,10 @@ bs_status bs_plan_check_groups(const bs_plan *plan, int64_t *bad_group);
 bs_status bs_contract(bs_plan *plan, const void *A, const void *B, void *C, void *stream);
 
 /* The same contraction on HOST buffers: copies A and B to plan-owned device
- * buffers (allocated on first use), contracts, copies C back into C_host
- * (which must hold the C layout's element count; only populated elements are
- * written) and synchronizes the stream before returning.  Pinned host memory
- * gives the fastest copies. */
+ * buffers (allocated on first use), contracts, copies the whole C buffer back
+ * into C_host (which must hold the C layout's element count; its padding and
+ * absent blocks receive zeros) and synchronizes the stream before returning.
+ * Pinned host memory gives the fastest copies. */
 bs_status bs_contract_host(bs_plan *plan, const void *A_host, const void *B_host, void *C_host,
                            void *stream);
 
