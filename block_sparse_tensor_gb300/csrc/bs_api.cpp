@@ -851,11 +851,23 @@ bs_status bs_contract_host(bs_plan *P, const void *A_host, const void *B_host, v
     BS_CUDA(cudaMalloc(&P->d_host_c, std::max<size_t>(nc, 16)));
     BS_CUDA(cudaMemset(P->d_host_c, 0, std::max<size_t>(nc, 16)));   // padding stays zero
   }
+  // A C buffer in pinned host memory that the device can address, under a plan
+  // that writes every C element once (no zero fill, no accumulation): the
+  // kernel stores C straight into it over the host link and no copy follows.
+  void *c_direct = nullptr;
+  if (P->zero_blocks.empty()) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, C_host) == cudaSuccess) {
+      if (at.type == cudaMemoryTypeHost && at.devicePointer) c_direct = at.devicePointer;
+    } else {
+      (void)cudaGetLastError();   // not a CUDA allocation: take the copy path
+    }
+  }
   BS_CUDA(cudaMemcpyAsync(P->d_host_a, A_host, na, cudaMemcpyHostToDevice, s));
   BS_CUDA(cudaMemcpyAsync(P->d_host_b, B_host, nb, cudaMemcpyHostToDevice, s));
-  bs_status st = bs_contract(P, P->d_host_a, P->d_host_b, P->d_host_c, stream);
+  bs_status st = bs_contract(P, P->d_host_a, P->d_host_b, c_direct ? c_direct : P->d_host_c, stream);
   if (st != BS_OK) return st;
-  BS_CUDA(cudaMemcpyAsync(C_host, P->d_host_c, nc, cudaMemcpyDeviceToHost, s));
+  if (!c_direct) BS_CUDA(cudaMemcpyAsync(C_host, P->d_host_c, nc, cudaMemcpyDeviceToHost, s));
   BS_CUDA(cudaStreamSynchronize(s));
   return BS_OK;
 }

@@ -210,12 +210,39 @@ def test_repeated_calls_are_identical():
     assert np.array_equal(c1, c2)          # one writer per C element: deterministic
 
 
-def test_host_buffer_entry_point_matches_device_entry_point():
-    r = Run(bsgen.config2())
+def _populated(run):
+    L = run.P.c_layout
+    mask = np.zeros(L.nelems, bool)
+    mask[L.element_index(L.blocks())] = True
+    return mask
+
+
+@pytest.mark.parametrize("pol", ["contraction", "free"])
+def test_host_buffer_entry_point_matches_device_entry_point(pol):
+    """Unpinned C: copied back whole (padding arrives as zeros).  Pinned C under a
+    write-once plan: the kernel stores into it and leaves padding untouched.  A
+    free-axis plan (zero fill, accumulation) always copies."""
+    r = Run(bsgen.config2(), None, None, "blockrow|align16", **POLICIES[pol])   # C rows padded to 16 bytes
     c_dev = r.run()
-    c_host = np.zeros(r.P.c_layout.nelems, np.float64)
+    pop = _populated(r)
+    assert (~pop).sum() > 0
+    # free-axis groups accumulate with atomics, so two runs may round differently
+    same = (np.array_equal if pol == "contraction" else
+            lambda x, y: np.allclose(x, y, rtol=1e-12, atol=1e-12 * np.abs(y).max()))
+    c_host = np.full(r.P.c_layout.nelems, np.nan)
     bs.contract_host(r.P, r.a_host, r.b_host, c_host)
-    assert np.array_equal(c_host, c_dev)
+    assert same(c_host[pop], c_dev[pop]) and np.all(c_host[~pop] == 0)
+    a_pin = torch.from_numpy(r.a_host).pin_memory()
+    b_pin = torch.from_numpy(r.b_host).pin_memory()
+    c_pin = torch.full((r.P.c_layout.nelems,), float("nan"), dtype=torch.float64).pin_memory()
+    for _ in range(2):
+        bs.contract_host(r.P, a_pin, b_pin, c_pin)
+        got = c_pin.numpy()
+        assert same(got[pop], c_dev[pop])
+        if pol == "contraction":
+            assert r.P.stats()["launches"] == 1 and np.all(np.isnan(got[~pop]))
+        else:
+            assert np.all(got[~pop] == 0)
 
 
 def test_uncoalesced_control_matches_oracle():
