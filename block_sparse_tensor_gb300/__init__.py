@@ -34,7 +34,7 @@ EXPORTED = ["bs_layout_create", "bs_layout_query", "bs_layout_blocks", "bs_layou
             "bs_plan_groups", "bs_plan_triples", "bs_contract", "bs_contract_host",
             "bs_contract_uncoalesced", "bs_plan_last_device_error", "bs_plan_destroy",
             "bs_status_string", "bs_version", "bs_calibrate", "bs_contract_noalloc",
-            "bs_plan_check_groups"]
+            "bs_plan_check_groups", "bs_plan_create_into"]
 
 
 class BsError(RuntimeError):
@@ -111,6 +111,7 @@ def _load(path: str = LIB_PATH):
         "bs_calibrate": (st, [P, P]),
         "bs_contract_noalloc": (st, [P, P, P, P, P]),
         "bs_plan_check_groups": (st, [P, P]),
+        "bs_plan_create_into": (st, [P, P, P, i32, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -243,10 +244,15 @@ def plan_options(**kw) -> PlanOptions:
 class Plan:
     """A contraction plan (bs_plan) for C = A B."""
 
-    def __init__(self, A: Layout, B: Layout, dtype: int = F64, **options):
+    def __init__(self, A: Layout, B: Layout, dtype: int = F64, C: Layout = None, **options):
+        """With C, plan onto that existing C layout (bs_plan_create_into)."""
         self.opts = plan_options(**options)
         h = ctypes.c_void_p()
-        _check(lib.bs_plan_create(A.h, B.h, int(dtype), ctypes.byref(self.opts), ctypes.byref(h)), "bs_plan_create")
+        if C is None:
+            _check(lib.bs_plan_create(A.h, B.h, int(dtype), ctypes.byref(self.opts), ctypes.byref(h)), "bs_plan_create")
+        else:
+            _check(lib.bs_plan_create_into(A.h, B.h, C.h, int(dtype), ctypes.byref(self.opts), ctypes.byref(h)),
+                   "bs_plan_create_into")
         self.h = h
         self.dtype = dtype
         self.c_layout = Layout(None, None, None, _handle=lib.bs_plan_c_layout(h), _owner=self)

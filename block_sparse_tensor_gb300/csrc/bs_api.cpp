@@ -395,8 +395,8 @@ void bs_plan_options_default(bs_plan_options *o) {
   o->merge_rows = 1;
 }
 
-bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, const bs_plan_options *opts,
-                         bs_plan **out) {
+static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_layout *Cg, int32_t dtype,
+                             const bs_plan_options *opts, bs_plan **out) {
   if (!out) return BS_ERR_INVALID_ARG;
   *out = nullptr;
   if (!A || !B) return BS_ERR_INVALID_ARG;
@@ -423,7 +423,29 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
     P->opts = o;
     P->A = *A;
     P->B = *B;
-    st = build_layout(A->rows, B->cols, product_sparsity(*A, *B), o.c_layout_flags, dtype == BS_F64 ? 8 : 4, &P->C);
+    if (Cg) {
+      // a caller's C layout: the same axes, the element size of the dtype's
+      // output and exactly the structural product as its populated set
+      st = BS_OK;
+      if (!Cg->rows.same_as(A->rows) || !Cg->cols.same_as(B->cols)) st = BS_ERR_SHAPE_MISMATCH;
+      else if (Cg->elem_bytes != (dtype == BS_F64 ? 8 : 4)) st = BS_ERR_INVALID_ARG;
+      else {
+        const Sparsity sp = product_sparsity(*A, *B);
+        if ((size_t)sp.ptr.back() != Cg->blocks.size()) st = BS_ERR_SHAPE_MISMATCH;
+        std::vector<int32_t> cols;
+        for (int32_t r = 0; st == BS_OK && r < Cg->rows.n; ++r) {
+          cols.clear();
+          for (int64_t t = Cg->row_ptr[r]; t < Cg->row_ptr[r + 1]; ++t) cols.push_back(Cg->blocks[Cg->row_blk[t]].col);
+          std::sort(cols.begin(), cols.end());
+          if (!std::equal(cols.begin(), cols.end(), sp.cols.begin() + sp.ptr[r], sp.cols.begin() + sp.ptr[r + 1]) ||
+              (int64_t)cols.size() != sp.ptr[r + 1] - sp.ptr[r])
+            st = BS_ERR_SHAPE_MISMATCH;
+        }
+      }
+      if (st == BS_OK) P->C = *Cg;
+    } else {
+      st = build_layout(A->rows, B->cols, product_sparsity(*A, *B), o.c_layout_flags, dtype == BS_F64 ? 8 : 4, &P->C);
+    }
     if (st != BS_OK) {
       delete P;
       return st;
@@ -624,6 +646,20 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, 
   P->stats.plan_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
   *out = P;
   return BS_OK;
+}
+
+bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, const bs_plan_options *opts,
+                         bs_plan **out) {
+  return plan_create(A, B, nullptr, dtype, opts, out);
+}
+
+bs_status bs_plan_create_into(const bs_layout *A, const bs_layout *B, const bs_layout *C, int32_t dtype,
+                              const bs_plan_options *opts, bs_plan **out) {
+  if (!C) {
+    if (out) *out = nullptr;
+    return BS_ERR_INVALID_ARG;
+  }
+  return plan_create(A, B, C, dtype, opts, out);
 }
 
 const bs_layout *bs_plan_c_layout(const bs_plan *P) { return P ? &P->C : nullptr; }

@@ -205,6 +205,15 @@ typedef struct bs_plan_stats {
 bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype,
                          const bs_plan_options *opts, bs_plan **out);
 
+/* The same plan onto a C layout the caller already has (a tensor to write
+ * into, another stage's layout): C's row axis must be A's, its column axis
+ * B's, and its populated blocks exactly the structural product, else
+ * BS_ERR_SHAPE_MISMATCH; its elem_bytes must be 8 for F64 and 4 for BF16_F32
+ * (INVALID_ARG otherwise).  The plan keeps its own copy of C's description
+ * (opts->c_layout_flags is not used); C may be destroyed afterwards. */
+bs_status bs_plan_create_into(const bs_layout *A, const bs_layout *B, const bs_layout *C, int32_t dtype,
+                              const bs_plan_options *opts, bs_plan **out);
+
 /* C's layout, owned by the plan (valid until bs_plan_destroy). */
 const bs_layout *bs_plan_c_layout(const bs_plan *plan);
 

@@ -245,6 +245,22 @@ def test_host_buffer_entry_point_matches_device_entry_point(pol):
             assert np.all(got[~pop] == 0)
 
 
+def test_plan_onto_a_given_c_layout_matches_oracle():
+    w = bsgen.config2()
+    lc = "colpanel|charge_sorted"
+    r = Run(w, None, None, lc)
+    c1 = r.run()
+    compare(r, c1)
+    C = bs.Layout(w.rows, w.cols, bsgen.Rule(-2, 2), lc, 8)
+    P2 = bs.Plan(r.A, r.B, bs.F64, C=C)
+    assert np.array_equal(P2.c_layout.blocks(), r.P.c_layout.blocks())
+    c2 = torch.full_like(r.c, float("nan"))
+    bs.contract(P2, r.a, r.b, c2)
+    torch.cuda.synchronize()
+    assert bs.last_device_error(P2) == 0
+    assert np.array_equal(c2.cpu().numpy(), c1, equal_nan=True)
+
+
 def test_uncoalesced_control_matches_oracle():
     r = Run(bsgen.config2())
     c = r.run(bs.contract_uncoalesced)

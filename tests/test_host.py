@@ -301,3 +301,28 @@ def test_bucket_padding_accounts_its_waste():
         assert bk.check_groups() == (0, -1)
     with pytest.raises(bs.BsError):
         host_plan(w, bucket_pad=2)
+
+
+def test_plan_onto_a_given_c_layout():
+    """bs_plan_create_into: a C layout equal to the structural product is taken as
+    given; a subset or superset of it, or the wrong element size, is refused."""
+    w = bsgen.config2()
+    A = bs.Layout(w.rows, w.inner, w.rule_a, w.layout_a, 8)
+    B = bs.Layout(w.inner, w.cols, w.rule_b, w.layout_b, 8)
+    C = bs.Layout(w.rows, w.cols, bsgen.Rule(-2, 2), "colpanel|charge_sorted", 8)   # |dq| <= 1 twice
+    P = bs.Plan(A, B, bs.F64, C=C, host_only=1)
+    assert P.c_layout.nelems == C.nelems and np.array_equal(P.c_layout.blocks(), C.blocks())
+    assert P.check_groups() == (0, -1)
+    want, _, _ = oracle_triples(w)
+    assert P.stats()["triples"] == len(want)
+    for rule in (bsgen.Rule(-1, 1), bsgen.Rule(-3, 3)):
+        with pytest.raises(bs.BsError) as e:
+            bs.Plan(A, B, bs.F64, C=bs.Layout(w.rows, w.cols, rule, "blockrow", 8), host_only=1)
+        assert e.value.code == 2
+    with pytest.raises(bs.BsError) as e:
+        bs.Plan(A, B, bs.F64, C=bs.Layout(w.rows, w.cols, bsgen.Rule(-2, 2), "blockrow", 4), host_only=1)
+    assert e.value.code == 1
+    other = bsgen.Axis(w.rows.q[:-1], w.rows.d[:-1])   # a row axis that is not A's
+    with pytest.raises(bs.BsError) as e:
+        bs.Plan(A, B, bs.F64, C=bs.Layout(other, w.cols, bsgen.Rule(-2, 2), "blockrow", 8), host_only=1)
+    assert e.value.code == 2
