@@ -259,7 +259,8 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f64", "data": "synthetic",
-        "blocks_per_s": blocks_s,
+        "blocks_per_s": blocks_s,   # populated (i, k, j) triples per second
+        "c_blocks_per_s": weak_scaling_value(st["c_blocks"], world, ms),
         "config": {"workload": workload_desc(w), "triples": st["triples"], "c_blocks": st["c_blocks"],
                    "useful_gflop": st["useful_flops"] / 1e9, "useful_mb": st["useful_bytes"] / 1e6,
                    "groups": st["groups"], "axis": ["auto", "contraction", "free", "none"][st["axis"]],
@@ -311,7 +312,8 @@ def per_config(bs, torch, flush, stream, calib, peaks, args, clock_mhz):
         assert bs.last_device_error(pb.P, stream) == 0
         rl = roofline(w, st, ms, calib, peaks, clock_mhz)
         rec = {"workload": w.name, "dtype": w.dtype, "ms": ms, "gflops": st["useful_flops"] / (ms * 1e-3) / 1e9,
-               "blocks_per_s": st["triples"] / (ms * 1e-3), "triples": st["triples"], "c_blocks": st["c_blocks"],
+               "blocks_per_s": st["triples"] / (ms * 1e-3), "c_blocks_per_s": st["c_blocks"] / (ms * 1e-3),
+               "triples": st["triples"], "c_blocks": st["c_blocks"],
                "groups": st["groups"], "tasks": st["tasks"], "useful_gflop": st["useful_flops"] / 1e9,
                "useful_mb": st["useful_bytes"] / 1e6, "roofline_frac": rl["frac"], "roofline_bound": rl["bound"],
                "executed_over_useful": st["executed_flops"] / max(st["useful_flops"], 1),
