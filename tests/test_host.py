@@ -326,3 +326,21 @@ def test_plan_onto_a_given_c_layout():
     with pytest.raises(bs.BsError) as e:
         bs.Plan(A, B, bs.F64, C=bs.Layout(other, w.cols, bsgen.Rule(-2, 2), "blockrow", 8), host_only=1)
     assert e.value.code == 2
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_structures_plan_exactly_and_hole_free(seed):
+    """Random small structures (repeated charges, optional parity, random band
+    rules): every policy covers the oracle's triples once, builds the oracle's C
+    layout and passes the group validator."""
+    w = bsgen.tiny_random(1000 + seed, max_sectors=10, max_dim=7)
+    want, _, _ = oracle_triples(w)
+    pr = oracle.problem(w)
+    for pol in POLICIES + [dict(axis_policy=bs.AXIS_CONTRACTION, merge_rows=1)]:
+        P, _, _ = host_plan(w, **pol)
+        ptr, tr = P.triples()
+        got = [tuple(int(x) for x in t) for t in tr]
+        assert len(got) == len(set(got)) and set(got) == want
+        assert P.check_groups() == (0, -1)
+        assert P.c_layout.nelems == pr.lc.nelems
+        assert np.array_equal(lib_blocks_by_rc(P.c_layout), pr.lc.blocks())
