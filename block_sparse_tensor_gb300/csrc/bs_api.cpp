@@ -899,8 +899,24 @@ bs_status bs_contract_host(bs_plan *P, const void *A_host, const void *B_host, v
       (void)cudaGetLastError();   // not a CUDA allocation: take the copy path
     }
   }
-  BS_CUDA(cudaMemcpyAsync(P->d_host_a, A_host, na, cudaMemcpyHostToDevice, s));
-  BS_CUDA(cudaMemcpyAsync(P->d_host_b, B_host, nb, cudaMemcpyHostToDevice, s));
+  // Inputs in pinned host memory that the device can address are pulled in by
+  // one copy kernel (a single launch, loads spread over the SMs); any other
+  // host memory goes through the copy engine, one copy per operand.
+  auto device_alias = [](const void *h) -> const void * {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+  };
+  const void *a_dev = device_alias(A_host), *b_dev = device_alias(B_host);
+  if (a_dev && b_dev && ((uintptr_t)a_dev | (uintptr_t)b_dev) % 16 == 0) {
+    BS_CUDA(launch_stage_in(a_dev, P->d_host_a, na, b_dev, P->d_host_b, nb, P->sm_count, s));
+  } else {
+    BS_CUDA(cudaMemcpyAsync(P->d_host_a, A_host, na, cudaMemcpyHostToDevice, s));
+    BS_CUDA(cudaMemcpyAsync(P->d_host_b, B_host, nb, cudaMemcpyHostToDevice, s));
+  }
   bs_status st = bs_contract(P, P->d_host_a, P->d_host_b, c_direct ? c_direct : P->d_host_c, stream);
   if (st != BS_OK) return st;
   if (!c_direct) BS_CUDA(cudaMemcpyAsync(C_host, P->d_host_c, nc, cudaMemcpyDeviceToHost, s));

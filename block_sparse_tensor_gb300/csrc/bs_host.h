@@ -49,11 +49,14 @@ bs_status build_layout(const AxisCopy &rows, const AxisCopy &cols, const Sparsit
 bs_status copy_axis(const bs_axis_desc *d, AxisCopy *out);
 Sparsity rule_sparsity(const AxisCopy &r, const AxisCopy &c, const bs_rule &rule);
 
-// Launchers (bs_fp64.cu, bs_bf16.cu).
+// Launchers (bs_fp64.cu, bs_bf16.cu, bs_stage.cu).
 cudaError_t launch_fp64_grouped(const Fp64Params &p, int grid, cudaStream_t s);
 cudaError_t launch_pack2(const PackParams &a, const PackParams &b, int32_t ntotal, int grid, cudaStream_t s);
 cudaError_t launch_zero(void *C, int elem_bytes, const ZeroBlock *blocks, int nblocks, int grid,
                         cudaStream_t s);
+// Copies n0 bytes src0 -> dst0 and n1 bytes src1 -> dst1 in one launch; every pointer 16-byte aligned.
+cudaError_t launch_stage_in(const void *src0, void *dst0, size_t n0, const void *src1, void *dst1, size_t n1, int sms,
+                            cudaStream_t s);
 cudaError_t launch_control_fp64(const double *A, const double *B, double *C, int64_t a_off, int64_t lda,
                                 int64_t b_off, int64_t ldb, int64_t c_off, int64_t ldc, int m, int n, int k,
                                 cudaStream_t s);

@@ -245,6 +245,29 @@ def test_host_buffer_entry_point_matches_device_entry_point(pol):
             assert np.all(got[~pop] == 0)
 
 
+@pytest.mark.parametrize("seed", [71, 75, 78, 81])
+def test_host_entry_point_staging_kernel_ragged_and_offset_inputs(seed):
+    """Pinned, 16-byte aligned A and B are pulled in by the staging kernel, whose
+    ragged last 8 bytes (operands with an odd element count) must arrive too; a
+    pinned operand that starts 8 bytes into its allocation takes the copy-engine
+    path.  Both give the device entry point's C bit for bit."""
+    w = bsgen.tiny_random(seed, values="int3", max_sectors=9, max_dim=23)
+    r = Run(w, "blockrow", "blockrow", "blockrow", **POLICIES["contraction"])
+    assert (r.A.nelems % 2) or (r.B.nelems % 2)
+    c_dev = r.run()
+    pop = _populated(r)
+    a_pin, b_pin = torch.from_numpy(r.a_host).pin_memory(), torch.from_numpy(r.b_host).pin_memory()
+    c_pin = torch.full((r.P.c_layout.nelems,), float("nan"), dtype=torch.float64).pin_memory()
+    bs.contract_host(r.P, a_pin, b_pin, c_pin)
+    assert np.array_equal(c_pin.numpy()[pop], c_dev[pop])
+    a_off = torch.zeros(r.A.nelems + 1, dtype=torch.float64).pin_memory()
+    a_off[1:] = torch.from_numpy(r.a_host)
+    c_pin.fill_(float("nan"))
+    bs.contract_host(r.P, a_off[1:], b_pin, c_pin)
+    assert np.array_equal(c_pin.numpy()[pop], c_dev[pop])
+    compare(r, c_pin.numpy().astype(np.float64), exact=True)
+
+
 def test_plan_onto_a_given_c_layout_matches_oracle():
     w = bsgen.config2()
     lc = "colpanel|charge_sorted"
