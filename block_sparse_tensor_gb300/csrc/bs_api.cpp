@@ -479,7 +479,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
     } else {
       P->sm_count = 152;
     }
-    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : (o.host_only ? 3 : std::max(1, fp64_max_ctas_per_sm()));
+    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : (o.host_only ? 3 : std::max(1, fp64_max_ctas_per_sm(false)));
     pm.parallel_ctas = P->sm_count * cps;
     pm.sms = P->sm_count;
 
@@ -634,7 +634,8 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
       }
       if (dtype == BS_F64) {
         const int64_t work_items = (int64_t)P->ts.tasks.size() + (int64_t)(P->ts.tail_elems.size() / 2 + kThreads - 1) / kThreads;
-        P->grid = (int)std::max<int64_t>(1, std::min<int64_t>(work_items, (int64_t)P->sm_count * cps));
+        const int launch_cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : fp64_max_ctas_per_sm(P->ts.tasks.empty());
+        P->grid = (int)std::max<int64_t>(1, std::min<int64_t>(work_items, (int64_t)P->sm_count * launch_cps));
       }
       else P->grid = std::max(1, (int)P->bctas.size());
     }

@@ -213,7 +213,12 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 4) fp64_grouped_kernel(Fp64Params p) {
+// Two instances: four CTAs per SM (64 registers a thread) for plans with tile
+// tasks, whose shared-memory staging wants the most resident warps, and three
+// (up to 85 registers) for plans made only of tail tasks, whose eight FMA
+// chains and their loads then stay in registers instead of spilling.
+template <int kMinCtas>
+__global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Params p) {
   __shared__ TileSmem sm;
   // tile tasks, one CTA each, longest first
   for (; p.ntasks > 0;) {
@@ -334,14 +339,17 @@ __global__ void control_bf16_kernel(const uint16_t *A, const uint16_t *B, float 
 }  // namespace
 
 cudaError_t launch_fp64_grouped(const Fp64Params &p, int grid, cudaStream_t s) {
-  fp64_grouped_kernel<<<grid, kThreads, 0, s>>>(p);
+  if (p.ntasks > 0) fp64_grouped_kernel<4><<<grid, kThreads, 0, s>>>(p);
+  else fp64_grouped_kernel<3><<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-int fp64_max_ctas_per_sm() {
+int fp64_max_ctas_per_sm(bool tail_only) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp64_grouped_kernel, kThreads, 0) != cudaSuccess) return 1;
-  return n;
+  const cudaError_t e = tail_only
+                            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp64_grouped_kernel<3>, kThreads, 0)
+                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp64_grouped_kernel<4>, kThreads, 0);
+  return e == cudaSuccess && n > 0 ? n : 1;
 }
 
 cudaError_t launch_pack2(const PackParams &a, const PackParams &b, int32_t ntotal, int grid, cudaStream_t s) {

@@ -63,7 +63,9 @@ cudaError_t launch_control_fp64(const double *A, const double *B, double *C, int
 cudaError_t launch_control_bf16(const uint16_t *A, const uint16_t *B, float *C, int64_t a_off, int64_t lda,
                                 int64_t b_off, int64_t ldb, int64_t c_off, int64_t ldc, int m, int n, int k,
                                 cudaStream_t s);
-int fp64_max_ctas_per_sm();
+// Resident CTAs per SM of the FP64 kernel instance a plan with (false) or
+// without (true) tile tasks launches.
+int fp64_max_ctas_per_sm(bool tail_only);
 
 struct Bf16Params {
   const void *maps;          // CUtensorMap array in device memory (64-byte aligned)

@@ -114,7 +114,7 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BS_ERR_CUDA;
-  per_sm = std::max(1, fp64_max_ctas_per_sm());
+  per_sm = std::max(1, fp64_max_ctas_per_sm(P->ts.tasks.empty()));
 
   auto up = [&](size_t o, const void *src, size_t n) -> bool {
     return n == 0 || cudaMemcpyAsync(b + o, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
