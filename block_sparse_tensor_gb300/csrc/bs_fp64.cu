@@ -128,7 +128,7 @@ __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
 // One output per lane for 32 consecutive outputs of the tail list.  The loop
 // count is the warp's longest K; a lane whose group is shorter stops adding.
 // When every lane's group is one view (the usual case with panel layouts) the
-// loop is unrolled with eight accumulators; otherwise each lane walks its
+// loop is unrolled with six accumulators; otherwise each lane walks its
 // group's views, switching view on its own.
 __device__ void run_tail_warp(const Fp64Params &p, int w) {
   const int lane = threadIdx.x & 31;
@@ -151,11 +151,12 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
     const int64_t ldb = D.ldb;
     cofs = D.c0 + (int64_t)r * D.ldc + c;
     flags = D.flags;
-    // eight independent chains with their loads issued ahead, so that a warp
-    // left alone on its SM at the end of the launch still keeps enough B rows
-    // in flight to feed the FP64 pipe; steps past this lane's K load nothing
+    // six independent chains with their loads issued ahead, so that a warp
+    // left alone on its SM at the end of the launch still keeps B rows in
+    // flight (six measure faster than eight or ten, which need more registers
+    // than four resident CTAs leave); steps past this lane's K load nothing
     // and add 0 * 0
-    constexpr int U = 8;
+    constexpr int U = 6;
     double a[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) a[u] = 0.0;
@@ -172,7 +173,7 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
     }
     for (; it < kmax; ++it)
       if (it < kg) a[0] = fma(__ldg(ap + it), __ldg(bp + it * ldb), a[0]);
-    acc = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+    acc = ((a[0] + a[1]) + (a[2] + a[3])) + (a[4] + a[5]);
   } else {
     // general path: walk the group's row and inner segments
     const Group G = p.groups[el.x];
@@ -215,8 +216,8 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
 
 // Two instances: four CTAs per SM (64 registers a thread) for plans with tile
 // tasks, whose shared-memory staging wants the most resident warps, and three
-// (up to 85 registers) for plans made only of tail tasks, whose eight FMA
-// chains and their loads then stay in registers instead of spilling.
+// for plans made only of tail tasks, which measure faster with fewer, quicker
+// CTAs sharing each SM.
 template <int kMinCtas>
 __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Params p) {
   __shared__ TileSmem sm;
