@@ -891,8 +891,11 @@ bs_status bs_contract_host(bs_plan *P, const void *A_host, const void *B_host, v
   // A C buffer in pinned host memory that the device can address, under a plan
   // that writes every C element once (no zero fill, no accumulation): the
   // kernel stores C straight into it over the host link and no copy follows.
+  // That saves the copy's fixed cost; past a few MiB the copy engine moves C
+  // faster than the kernel's stores do, so larger C takes the copy.
+  constexpr size_t kDirectCBytes = (size_t)4 << 20;
   void *c_direct = nullptr;
-  if (P->zero_blocks.empty()) {
+  if (P->zero_blocks.empty() && nc <= kDirectCBytes) {
     cudaPointerAttributes at{};
     if (cudaPointerGetAttributes(&at, C_host) == cudaSuccess) {
       if (at.type == cudaMemoryTypeHost && at.devicePointer) c_direct = at.devicePointer;

@@ -261,11 +261,11 @@ bs_status bs_contract(bs_plan *plan, const void *A, const void *B, void *C, void
  * When A_host and B_host are both 16-byte aligned pinned host memory the
  * device can address (cudaHostAlloc, cudaHostRegister), one copy kernel pulls
  * them in; otherwise each goes through the copy engine.  When C_host is pinned
- * host memory the device can address and the plan writes each C element once
- * (no zero fill), the kernel stores C straight into C_host: every populated
- * element is written and the rest of C_host is left unchanged.  Otherwise the
- * whole C buffer is copied back and its padding and absent blocks arrive as
- * zeros.  Pinned host memory gives the fastest calls. */
+ * host memory the device can address, the plan writes each C element once (no
+ * zero fill) and C takes at most 4 MiB, the kernel stores C straight into
+ * C_host: every populated element is written and the rest of C_host is left
+ * unchanged.  Otherwise the whole C buffer is copied back and its padding and
+ * absent blocks arrive as zeros.  Pinned host memory gives the fastest calls. */
 bs_status bs_contract_host(bs_plan *plan, const void *A_host, const void *B_host, void *C_host,
                            void *stream);
 

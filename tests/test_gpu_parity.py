@@ -245,6 +245,21 @@ def test_host_buffer_entry_point_matches_device_entry_point(pol):
             assert np.all(got[~pop] == 0)
 
 
+def test_host_entry_point_large_pinned_c_is_copied_back():
+    """A pinned C larger than 4 MiB (workload 4: 55 MB of FP32) is not stored into
+    directly: it arrives by one copy of the whole buffer, padding as zeros."""
+    r = Run(bsgen.config4())
+    c_dev = r.run()
+    pop = _populated(r)
+    assert (~pop).sum() > 0 and r.P.c_layout.nelems * 4 > (4 << 20)
+    a_pin = torch.from_numpy(r.a_host.view(np.int16)).pin_memory()
+    b_pin = torch.from_numpy(r.b_host.view(np.int16)).pin_memory()
+    c_pin = torch.full((r.P.c_layout.nelems,), float("nan"), dtype=torch.float32).pin_memory()
+    bs.contract_host(r.P, a_pin, b_pin, c_pin)
+    got = c_pin.numpy()
+    assert np.array_equal(got[pop], c_dev[pop]) and np.all(got[~pop] == 0)
+
+
 @pytest.mark.parametrize("seed", [71, 75, 78, 81])
 def test_host_entry_point_staging_kernel_ragged_and_offset_inputs(seed):
     """Pinned, 16-byte aligned A and B are pulled in by the staging kernel, whose
