@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <future>
 #include <map>
 #include <new>
 #include <tuple>
@@ -500,57 +501,89 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
       double best = 1e300;
       int best_axis = -1;
       bool best_pack = false;
+      // Every (axis, pack) candidate is built and costed on its own thread;
+      // the cheapest in this order wins, the first of equals.
+      struct Built {
+        int ax = 0;
+        bool pk = false;
+        bs_status st = BS_OK;
+        bs_layout Apk, Bpk;
+        GroupSet gs;
+        TileSet ts;
+        double us = 0, ms_group = 0, ms_tile = 0;
+      };
+      std::vector<Built> built;
       for (int ax : axes)
         for (bool pk : packs) {
           if (pk && ax == BS_AXIS_NONE) continue;
-          bs_layout Apk, Bpk;
-          const bs_layout *Ae = &P->A, *Be = &P->B;
-          int64_t pbytes = 0;
-          if (pk) {
-            st = packed(P->A, ax == BS_AXIS_FREE ? BS_LAYOUT_COLPANEL : BS_LAYOUT_ROWPANEL, &Apk);
-            if (st != BS_OK) break;
-            Ae = &Apk;
-            pbytes += populated_elems(P->A) * eb_in;
-            if (ax == BS_AXIS_CONTRACTION) {
-              st = packed(P->B, BS_LAYOUT_COLPANEL, &Bpk);
-              if (st != BS_OK) break;
-              Be = &Bpk;
-              pbytes += populated_elems(P->B) * eb_in;
-            }
-          }
-          const auto tg0 = std::chrono::steady_clock::now();
-          GroupSet gs = ax == BS_AXIS_CONTRACTION ? make_contraction_groups(*Ae, *Be, P->C, o.merge_rows != 0, false, unchecked)
-                        : ax == BS_AXIS_FREE      ? make_free_groups(*Ae, *Be, P->C)
-                                                  : make_triple_groups(*Ae, *Be, P->C);
-          const auto tg1 = std::chrono::steady_clock::now();
-          TileSet ts;
-          tile_fp64(gs, pm, &ts);
-          const auto tg2 = std::chrono::steady_clock::now();
-          const bool atomic = ax != BS_AXIS_CONTRACTION;
-          const int launches = 1 + (pk ? 1 : 0) + (atomic ? 1 : 0);
-          const double us = model_fp64_us(gs, ts, pm, pbytes, launches);
-          if (std::getenv("BS_LOG"))
-            std::fprintf(stderr, "[bs] candidate axis=%d pack=%d groups=%zu tasks=%zu model=%.1f us (group %.1f ms, tile %.1f ms)\n",
-                         ax, (int)pk, gs.groups.size(), ts.tasks.size(), us,
-                         std::chrono::duration<double, std::milli>(tg1 - tg0).count(),
-                         std::chrono::duration<double, std::milli>(tg2 - tg1).count());
-          cands.push_back({ax, pk, us});
-          if (us < best) {
-            best = us;
-            best_axis = ax;
-            best_pack = pk;
-            P->gs = std::move(gs);
-            P->ts = std::move(ts);
-            P->pack_a = pk;
-            P->pack_b = pk && ax == BS_AXIS_CONTRACTION;
-            if (pk) P->A_pk = Apk;
-            if (P->pack_b) P->B_pk = Bpk;
+          built.emplace_back();
+          built.back().ax = ax;
+          built.back().pk = pk;
+        }
+      const bool only = built.size() == 1;   // a single candidate is the plan
+      auto build_one = [&](Built &c) {
+        const int ax = c.ax;
+        const bool pk = c.pk;
+        const bs_layout *Ae = &P->A, *Be = &P->B;
+        int64_t pbytes = 0;
+        if (pk) {
+          c.st = packed(P->A, ax == BS_AXIS_FREE ? BS_LAYOUT_COLPANEL : BS_LAYOUT_ROWPANEL, &c.Apk);
+          if (c.st != BS_OK) return;
+          Ae = &c.Apk;
+          pbytes += populated_elems(P->A) * eb_in;
+          if (ax == BS_AXIS_CONTRACTION) {
+            c.st = packed(P->B, BS_LAYOUT_COLPANEL, &c.Bpk);
+            if (c.st != BS_OK) return;
+            Be = &c.Bpk;
+            pbytes += populated_elems(P->B) * eb_in;
           }
         }
+        const auto tg0 = std::chrono::steady_clock::now();
+        c.gs = ax == BS_AXIS_CONTRACTION ? make_contraction_groups(*Ae, *Be, P->C, o.merge_rows != 0, false, unchecked)
+               : ax == BS_AXIS_FREE      ? make_free_groups(*Ae, *Be, P->C)
+                                         : make_triple_groups(*Ae, *Be, P->C);
+        const auto tg1 = std::chrono::steady_clock::now();
+        tile_fp64(c.gs, pm, &c.ts, only);
+        const auto tg2 = std::chrono::steady_clock::now();
+        const bool atomic = ax != BS_AXIS_CONTRACTION;
+        const int launches = 1 + (pk ? 1 : 0) + (atomic ? 1 : 0);
+        c.us = model_fp64_us(c.gs, c.ts, pm, pbytes, launches);
+        c.ms_group = std::chrono::duration<double, std::milli>(tg1 - tg0).count();
+        c.ms_tile = std::chrono::duration<double, std::milli>(tg2 - tg1).count();
+      };
+      if (only) {
+        build_one(built[0]);
+      } else {
+        std::vector<std::future<void>> running;
+        for (auto &c : built) running.push_back(std::async(std::launch::async, build_one, std::ref(c)));
+        for (auto &f : running) f.get();
+      }
+      for (auto &c : built) {
+        if (c.st != BS_OK) {
+          st = c.st;
+          break;
+        }
+        if (std::getenv("BS_LOG"))
+          std::fprintf(stderr, "[bs] candidate axis=%d pack=%d groups=%zu tasks=%zu model=%.1f us (group %.1f ms, tile %.1f ms)\n",
+                       c.ax, (int)c.pk, c.gs.groups.size(), c.ts.tasks.size(), c.us, c.ms_group, c.ms_tile);
+        cands.push_back({c.ax, c.pk, c.us});
+        if (c.us < best) {
+          best = c.us;
+          best_axis = c.ax;
+          best_pack = c.pk;
+          P->gs = std::move(c.gs);
+          P->ts = std::move(c.ts);
+          P->pack_a = c.pk;
+          P->pack_b = c.pk && c.ax == BS_AXIS_CONTRACTION;
+          if (c.pk) P->A_pk = c.Apk;
+          if (P->pack_b) P->B_pk = c.Bpk;
+        }
+      }
       if (st != BS_OK) {
         delete P;
         return st;
       }
+      if (!only) tile_fp64(P->gs, pm, &P->ts, true);   // the chosen candidate in full
       P->axis = best_axis;
       P->stats.model_us = best;
       double alt = 0;

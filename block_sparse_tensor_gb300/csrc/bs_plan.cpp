@@ -304,12 +304,13 @@ static void tile_shape(int32_t m, int32_t n, int32_t area, int32_t *tm, int32_t 
 
 static inline int64_t lanes(int64_t e) { return (e + 31) / 32 * 32; }
 
-void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
+void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize) {
   ts->tasks.clear();
   ts->tail_elems.clear();
   ts->tq_ptr.clear();
   ts->tq_items.clear();
-  ts->tdesc.assign(gs.groups.size(), TailDesc{});
+  ts->tdesc.clear();
+  if (materialize) ts->tdesc.assign(gs.groups.size(), TailDesc{});
   std::vector<std::pair<double, Task>> costed;
   std::vector<int32_t> tails;
   double exec = 0, work = 0;
@@ -364,6 +365,23 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts) {
     if (!pm.bucket_pad) return ka > kb;   // exact: by K only, as listed
     return std::make_tuple(-ka, ma, na) < std::make_tuple(-kb, mb, nb);
   });
+  if (!materialize) {
+    // The executed flops of the tail list without listing it: each warp of
+    // 32 consecutive outputs runs its first output's K, and the outputs of
+    // the sorted groups follow one another.
+    int64_t off = 0;
+    for (int32_t g : tails) {
+      int32_t mp, np, kp;
+      padded(g, &mp, &np, &kp);
+      const int64_t end = off + (int64_t)mp * np;
+      const int64_t warps = (end + 31) / 32 - (off + 31) / 32;   // warp starts inside [off, end)
+      exec += 2.0 * 32.0 * kp * (double)warps;
+      off = end;
+    }
+    for (auto &c : costed) ts->tasks.push_back(c.second);
+    ts->executed_flops = exec;
+    return;
+  }
   std::vector<int32_t> elem_k;
   for (int32_t g : tails) {
     const Group &G = gs.groups[g];

@@ -45,7 +45,11 @@ GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const b
 GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C);
 GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C);
 void group_triples(const GroupSet &gs, std::vector<int64_t> *ptr, std::vector<int32_t> *out);
-void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts);
+// With materialize = false only what the cost model reads is produced: the
+// tile tasks (unsorted) and the executed flops; the tail list, its
+// descriptors and queues are left empty.  The planner costs every candidate
+// that way and materializes the chosen one.
+void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize = true);
 double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm, int64_t pack_bytes, int launches);
 
 // Host description of one TMA tensor map of the BF16 path (encoded per call
