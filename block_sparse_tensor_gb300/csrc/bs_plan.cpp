@@ -166,8 +166,27 @@ GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layou
   GroupSet &gs = bd.gs;
   gs.tptr.push_back(0);
   const int32_t nk = A.cols.n;
+  int64_t ntr = 0, ngr = 0;
+  for (int32_t k = 0; k < nk; ++k) {
+    const int64_t nb = B.row_ptr[k + 1] - B.row_ptr[k];
+    ntr += (A.col_ptr[k + 1] - A.col_ptr[k]) * nb;
+    if (A.col_ptr[k] != A.col_ptr[k + 1]) ngr += nb;
+  }
+  gs.triples.reserve((size_t)ntr * 3);
+  gs.rsegs.reserve((size_t)ntr);
+  gs.groups.reserve((size_t)ngr);
+  gs.ksegs.reserve((size_t)ngr);
+  gs.tptr.reserve((size_t)ngr + 1);
+  std::vector<int32_t> cblk;   // C block of (t-th A block of column k, u-th B block of row k)
   for (int32_t k = 0; k < nk; ++k) {
     if (A.col_ptr[k] == A.col_ptr[k + 1]) continue;
+    const int64_t na = A.col_ptr[k + 1] - A.col_ptr[k], nb = B.row_ptr[k + 1] - B.row_ptr[k];
+    // look the C blocks up row by row (each C row's blocks lie together)
+    cblk.resize((size_t)(na * nb));
+    for (int64_t t = 0; t < na; ++t) {
+      const int32_t i = A.blocks[A.col_blk[A.col_ptr[k] + t]].row;
+      for (int64_t u = 0; u < nb; ++u) cblk[t * nb + u] = C.find(i, B.blocks[B.row_blk[B.row_ptr[k] + u]].col);
+    }
     for (int64_t u = B.row_ptr[k]; u < B.row_ptr[k + 1]; ++u) {
       const auto &b = B.blocks[B.row_blk[u]];
       const int32_t j = b.col;
@@ -180,7 +199,7 @@ GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layou
       for (int64_t t = A.col_ptr[k]; t < A.col_ptr[k + 1]; ++t) {
         const auto &a = A.blocks[A.col_blk[t]];
         const int32_t i = a.row;
-        const auto &c = C.blocks[C.find(i, j)];
+        const auto &c = C.blocks[cblk[(t - A.col_ptr[k]) * nb + (u - B.row_ptr[k])]];
         bool join = false;
         if ((int32_t)gs.rsegs.size() > g.rseg_begin) {
           RowSeg &s = gs.rsegs.back();
