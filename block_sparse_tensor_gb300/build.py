@@ -17,7 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbs.so")
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I" + os.path.join(ROOT, "include")]
+COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-pthread", "-I" + os.path.join(ROOT, "include")]
 
 
 def sources():
@@ -56,7 +56,7 @@ def build(verbose_ptxas: bool = False) -> str:
         objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
     if os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest(objs):
         return LIB
-    cmd = [NVCC, *ARCH, "-shared", "-o", LIB + ".tmp", *objs]
+    cmd = [NVCC, *ARCH, "-shared", "-Xcompiler", "-pthread", "-o", LIB + ".tmp", *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -12,6 +12,7 @@
 #include <future>
 #include <map>
 #include <new>
+#include <system_error>
 #include <tuple>
 
 #include "bs_plan.h"
@@ -555,8 +556,17 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
         build_one(built[0]);
       } else {
         std::vector<std::future<void>> running;
-        for (auto &c : built) running.push_back(std::async(std::launch::async, build_one, std::ref(c)));
+        size_t started = 0;
+        try {
+          for (auto &c : built) {
+            running.push_back(std::async(std::launch::async, build_one, std::ref(c)));
+            ++started;
+          }
+        } catch (const std::system_error &) {
+          // no thread to be had: the remaining candidates are built here
+        }
         for (auto &f : running) f.get();
+        for (size_t c = started; c < built.size(); ++c) build_one(built[c]);
       }
       for (auto &c : built) {
         if (c.st != BS_OK) {
