@@ -2,9 +2,10 @@
 
 Each pin checks the oracle against something fixed by the pages or by
 mathematics: hand-derived golden fixtures (tests/golden), a dense embedding
-multiplied by numpy's matmul, charge conservation, closed forms for all-ones
-inputs, the one-sector case that is a textbook GEMM, and exactness of integer
-arithmetic.  The last test plants mistakes in copies of the oracle's C source
+multiplied by numpy's matmul (for C, and for the conditioning scale S, which
+must equal the dense product of the elementwise magnitudes |A| |B|), charge
+conservation, closed forms for all-ones inputs, the one-sector case that is a
+textbook GEMM, and exactness of integer arithmetic.  The last test plants mistakes in copies of the oracle's C source
 and requires that every planted mistake trips at least one pin.
 """
 import json
@@ -52,6 +53,9 @@ def check_dense_embedding(w, la=None, lb=None, lc=None, exact=False, rtol=1e-14)
     DA, ri, ki = dense_operand(w, 0, w.rows, w.inner, w.rule_a)
     DB, _, cj = dense_operand(w, 1, w.inner, w.cols, w.rule_b)
     DC = DA @ DB
+    # the conditioning scale: S = sum over the same terms of |a| |b|, i.e. the
+    # dense product of the elementwise magnitudes, restricted to populated C
+    DS = np.abs(DA) @ np.abs(DB)
     # the oracle's operand buffers hold exactly the seeded blocks
     for (r, c) in zip(*np.nonzero(pr.ma)):
         blk = oracle.block_view(pr.A, pr.la, r, c)
@@ -68,13 +72,18 @@ def check_dense_embedding(w, la=None, lb=None, lc=None, exact=False, rtol=1e-14)
                     fails.append(f"C block {i},{j} absent from the oracle but nonzero in the dense product")
                 continue
             got = oracle.block_view(C, pr.lc, i, j)
+            s = oracle.block_view(S, pr.lc, i, j)
+            sref = DS[ri[i]:ri[i + 1], cj[j]:cj[j + 1]]
             if exact:
                 if not np.array_equal(got, ref):
                     fails.append(f"C block {i},{j} differs (exact)")
+                if not np.array_equal(s, sref):
+                    fails.append(f"S block {i},{j} differs from |A| |B| (exact)")
             else:
-                s = oracle.block_view(S, pr.lc, i, j)
                 if np.linalg.norm(got - ref) > rtol * max(np.linalg.norm(s), 1e-300):
                     fails.append(f"C block {i},{j} differs beyond {rtol} of its scale")
+                if np.linalg.norm(s - sref) > rtol * max(np.linalg.norm(sref), 1e-300):
+                    fails.append(f"S block {i},{j} differs from |A| |B| beyond {rtol}")
     return fails
 
 
@@ -263,6 +272,8 @@ MUTANTS = {
     "charge_order_reversed": ("int before = q[v] < q[w]", "int before = q[v] > q[w]"),
     "bf16_widening_shift": ("<< 16;", "<< 15;"),
     "parity_ignored": ("if (z2 && ok) ok = rp[r] == cp[c];", "(void)rp; (void)cp;"),
+    "scale_drops_magnitude": ("mag = mag + (prod < 0 ? -prod : prod);", "mag = mag + prod;"),
+    "scale_skips_first_term": ("mag = mag + (prod < 0 ? -prod : prod);", "if (u + p > 0) mag = mag + (prod < 0 ? -prod : prod);"),
 }
 
 
