@@ -63,3 +63,55 @@ def check_blocks(c_got, c_ref, s_ref, blocks, tol):
     rel = np.where((ref == 0) & (sc == 0), err, rel)
     worst = float(rel.max()) if len(rel) else 0.0
     return worst <= tol, worst, int(cancel.sum())
+
+
+# ---------------------------------------------------------------- the oracle over every host core
+_POOL_PR = None
+
+
+def _pool_init(w, flags):
+    global _POOL_PR
+    _POOL_PR = oracle.problem(w, *flags)
+
+
+def _pool_blocks(sel):
+    """Oracle C and S values of the listed (i, j) blocks, concatenated block after
+    block (row-major inside a block), in the order of `sel`."""
+    C, S = oracle.contract(_POOL_PR, sel=sel)
+    lc = _POOL_PR.lc
+    blk = np.array([[i, j, lc.off[i, j], lc.rows[i], lc.cols[j], lc.ld[i, j]] for i, j in sel], np.int64)
+    idx = element_index(blk)
+    return C[idx], S[idx]
+
+
+def oracle_all_blocks(w, la, lb, lc, workers: int = 0):
+    """(C, S, problem) of the whole workload, its C blocks dealt longest-first by
+    flops over spawned worker processes (spawned, so none inherits a CUDA context);
+    each worker runs the plain oracle on its blocks."""
+    import multiprocessing as mp
+    import os
+    pr = oracle.problem(w, la, lb, lc)
+    ij = np.argwhere(pr.mc)
+    if len(ij) == 0:
+        return np.zeros(pr.lc.nelems), np.zeros(pr.lc.nelems), pr
+    kd = pr.ma.astype(np.float64) * w.inner.d[None, :].astype(np.float64)    # d_k where A[i,k]
+    ksum = kd @ pr.mb.astype(np.float64)                                      # sum of d_k over shared k
+    cost = w.rows.d[ij[:, 0]].astype(np.float64) * w.cols.d[ij[:, 1]] * ksum[ij[:, 0], ij[:, 1]]
+    n = max(1, min(workers or len(os.sched_getaffinity(0)), len(ij)))
+    load = np.zeros(n)
+    parts = [[] for _ in range(n)]
+    for t in np.argsort(-cost, kind="stable"):
+        b = int(np.argmin(load))
+        load[b] += cost[t]
+        parts[b].append(ij[t])
+    parts = [np.asarray(p, np.int32).reshape(-1, 2) for p in parts if p]
+    C = np.zeros(pr.lc.nelems)
+    S = np.zeros(pr.lc.nelems)
+    with mp.get_context("spawn").Pool(len(parts), initializer=_pool_init, initargs=(w, (la, lb, lc))) as pool:
+        for sel, (cv, sv) in zip(parts, pool.map(_pool_blocks, parts, chunksize=1)):
+            lcb = pr.lc
+            blk = np.array([[i, j, lcb.off[i, j], lcb.rows[i], lcb.cols[j], lcb.ld[i, j]] for i, j in sel], np.int64)
+            idx = element_index(blk)
+            C[idx] = cv
+            S[idx] = sv
+    return C, S, pr

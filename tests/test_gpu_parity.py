@@ -66,6 +66,7 @@ def compare(run: Run, c_got: np.ndarray, sel=None, exact=False):
         blocks = np.array([b for b in lib_c if (int(b[0]), int(b[1])) in keep])
     tol = 0.0 if exact else TOL[run.w.dtype]
     ok, worst, ncancel = check_blocks(c_got, C, S, blocks, tol)
+    print(f"[parity] {run.w.name}: {len(blocks)} blocks, worst {worst:.3e}, {ncancel} judged against ||S||")
     assert ok, f"worst per-block relative error {worst:.3e} > {tol} ({ncancel} cancelling blocks)"
     return worst
 
@@ -316,25 +317,87 @@ def test_bf16_wait_timeout_is_reported_and_context_survives():
     compare(r2, r2.run(), sel=sample_blocks(r2, 2e8, n_random=60))
 
 
-# ---------------------------------------------------------------- full-size workloads, sampled blocks
+# ---------------------------------------------------------------- integer inputs on the large-block paths
+def _int_workload(seed, dtype, rows_d, inner_d, cols_d, name):
+    """Three short band axes with large sectors: charges 0, 1, 2, ... (repeats allowed),
+    |dq| <= 1 for both operands, integer values in -3..3 (exact in any order)."""
+    rng = np.random.default_rng(seed)
+
+    def axis(ds):
+        q = np.sort(rng.integers(0, 3, len(ds)))
+        return bsgen.Axis(q, np.array(ds))
+
+    return bsgen.Workload(name, dtype, axis(rows_d), axis(inner_d), axis(cols_d), bsgen.Rule(-1, 1),
+                          bsgen.Rule(-1, 1), "int3", 0x1A7E0000 + seed)
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("pol", ["contraction", "free", "contraction_pack", "auto"])
+@pytest.mark.parametrize("lay", ["panels", "blockrow"])
+def test_fp64_tile_path_integer_inputs_bit_exact(seed, pol, lay):
+    """C blocks of more than 4096 outputs take the shared-memory tile path; their
+    K runs over several inner blocks (several views with block-row layouts) and
+    more than 16 chunks of 16.  Integer inputs: bit-exact in any summation order."""
+    rng = np.random.default_rng(100 + seed)
+    w = _int_workload(seed, "f64", rng.integers(60, 130, 4), rng.integers(60, 130, 5), rng.integers(65, 130, 3),
+                      f"int_tiles_{seed}")
+    r = Run(w, *LAYOUTS[lay], **POLICIES[pol])
+    st = r.P.stats()
+    assert st["tile_tasks"] > 0, "the case must reach the tile path"
+    assert max(g[3] for g in r.P.groups()) > 16 * 16 or st["axis"] == bs.AXIS_FREE
+    compare(r, r.run(), exact=True)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bf16_multi_tile_integer_inputs_bit_exact(seed):
+    """Groups of several 128-row M tiles, tile widths of 192 to 256 columns plus a
+    ragged second column tile, and K of more than four 64-deep stages over several
+    inner blocks.  Integers in -3..3 are exact in bfloat16 and every FP32 partial
+    sum stays exact, so the result must match bit for bit."""
+    rng = np.random.default_rng(200 + seed)
+    cols = [int(rng.integers(192, 257)), int(rng.integers(257, 330)), int(rng.integers(20, 100))]
+    w = _int_workload(seed, "bf16", rng.integers(130, 400, 3), rng.integers(70, 200, 4), cols, f"int_bf16_{seed}")
+    r = Run(w, "rowpanel|charge_sorted|align16", "colpanel|charge_sorted|align16", "rowpanel|align16")
+    st = r.P.stats()
+    g = r.P.groups()
+    assert st["tasks"] > st["groups"], "some group must span several tiles"
+    assert g[:, 1].max() > 128 and g[:, 2].max() > 256 and g[:, 3].max() > 256
+    compare(r, r.run(), exact=True)
+    r2 = Run(w, "blockrow", "blockrow", "blockrow", pack_policy=bs.PACK_ALWAYS)   # gathered into aligned panels
+    compare(r2, r2.run(), exact=True)
+
+
+# ---------------------------------------------------------------- full-size workloads, every block
+def compare_all(run: Run, c_got: np.ndarray):
+    """Every C block of a full-size workload against the oracle, run over every host core."""
+    from harness import oracle_all_blocks
+    C, S, pr = oracle_all_blocks(run.w, run.la, run.lb, run.lc)
+    lib_c = sort_rc(run.P.c_layout.blocks())
+    assert np.array_equal(lib_c, pr.lc.blocks()), "C block table differs from the oracle's"
+    tol = TOL[run.w.dtype]
+    ok, worst, ncancel = check_blocks(c_got, C, S, lib_c, tol)
+    print(f"[parity] {run.w.name}: all {len(lib_c)} blocks, worst {worst:.3e}, {ncancel} judged against ||S||")
+    assert ok, f"worst per-block relative error {worst:.3e} > {tol} ({ncancel} cancelling blocks)"
+
+
 @pytest.mark.parametrize("cfg", [3, 4, 5])
-def test_full_size_sampled_blocks(cfg):
+def test_full_size_every_block(cfg):
     w = bsgen.get(cfg)
     r = Run(w)
     c = r.run()
     from harness import element_index
     assert not np.any(np.isnan(c[element_index(r.P.c_layout.blocks())]))   # every populated element written
-    compare(r, c, sel=sample_blocks(r, 1.5e9 if cfg != 5 else 2.5e9, seed=cfg))
+    compare_all(r, c)
 
 
-def test_config5_pack_path_sampled_blocks():
+def test_config5_pack_path_every_block():
     w = bsgen.config5()
     r = Run(w, "blockrow", "blockrow", "blockrow", axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)
-    compare(r, r.run(), sel=sample_blocks(r, 1.0e9, seed=11))
+    compare_all(r, r.run())
 
 
-def test_config4_blockrow_gather_path_sampled_blocks():
+def test_config4_blockrow_gather_path_every_block():
     w = bsgen.config4()
     r = Run(w, w.pack_layout_a, w.pack_layout_b, w.pack_layout_c)
     assert r.P.stats()["packed_a"] == 1
-    compare(r, r.run(), sel=sample_blocks(r, 1.0e9, seed=4))
+    compare_all(r, r.run())
