@@ -2,13 +2,16 @@
 """Benchmark of the coalesced block-sparse contraction C[i,j] = sum_k A[i,k] B[k,j].
 
 One step = one bs_contract over the headline workload (default: the FP64
-"tail" workload of 31 U(1) sectors per axis, d(q) = max(1, round(64 e^{-q^2/50}))),
-inputs resident in HBM, L2 flushed between steps by a 256 MiB write.  Prints
-one JSON line: useful GFLOP/s (sum over populated triples of 2 d_i d_k d_j per
-second), blocks/s (populated triples per second), the roofline of the grouped
-kernel, an end-to-end number through the host-buffer entry point, the CPU
-oracle on the host cores, sampled clocks, and a per-workload summary of all
-five synthetic workloads with the one-launch-per-triple control beside them.
+launch-bound stress workload, 2000 random Z2 x U(1) sectors per axis with dims
+1..8 and sixteen sectors of 1024, 4.7 M populated block triples, 455 MB of
+operands and output), inputs resident in HBM, L2 flushed between steps by a
+256 MiB write (the inputs are larger than L2 as well).  Prints one JSON line:
+useful GFLOP/s (sum over populated triples of 2 d_i d_k d_j per second),
+blocks/s (populated triples per second), the roofline of the grouped kernel,
+an end-to-end number through the host-buffer entry point, the CPU oracle on
+the host cores, the one-launch-per-triple control, sampled clocks, and a
+per-workload summary of the other synthetic workloads, the chained
+contraction, bucketing and the gather kernel.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--config n]
 
@@ -127,10 +130,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------- GPU arm
+PLAN_OPTS = {}   # cost-model constants measured on the device (bs_calibrate), given to every plan
+
+
 class Problem:
     """Layouts, plan and resident device buffers of one workload."""
 
     def __init__(self, bs, torch, w: bsgen.Workload, **opts):
+        opts = {**PLAN_OPTS, **opts}
         self.w = w
         eb = 2 if w.dtype == "bf16" else 8
         self.A = bs.Layout(w.rows, w.inner, w.rule_a, w.layout_a, eb)
@@ -189,22 +196,44 @@ def recorded_traffic(workload: str, tag: str):
     return None
 
 
+def fp64_nominal_tflops():
+    return NOMINAL_SMS * FP64_FLOP_PER_CLK_PER_SM * NOMINAL_MAX_MHZ * 1e6 / 1e12
+
+
 def roofline(w, stats, kernel_ms, calib, peaks, clock_mhz):
     if w.dtype == "bf16":
         # BF16 workload: intensity below the tensor ridge, so HBM bounds it
         hbm = peaks.get("hbm_gbs") or 6800.0
         achieved = stats["useful_bytes"] / (kernel_ms * 1e-3) / 1e9
         out = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-               "peak_source": "MEASURED_PEAKS.json hbm_gbs" if peaks.get("hbm_gbs") else "fallback 6.8 TB/s"}
+               "peak_source": "of measured: MEASURED_PEAKS.json hbm_gbs" if peaks.get("hbm_gbs") else "of fallback 6.8 TB/s"}
     else:
-        peak = NOMINAL_SMS * FP64_FLOP_PER_CLK_PER_SM * NOMINAL_MAX_MHZ * 1e6 / 1e12
+        # The FP64 pipe: 4 flop per SM clock at the maximum SM clock.  The probes
+        # (bs_calibrate: FMA chains and the FP64 matrix instruction) measure the
+        # rate at the clock the part holds under that load, which is lower; the
+        # nominal figure is kept as the denominator because it is the higher one.
+        peak = fp64_nominal_tflops()
         achieved = stats["useful_flops"] / (kernel_ms * 1e-3) / 1e12
         out = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-               "peak_source": "FP64 pipe: 152 SMs x 4 flop/clk x 2070 MHz (nominal 1.25 TFLOP/s)",
-               "fp64_probe_tflops": calib["fp64_gflops"] / 1e3 if calib else None}
+               "peak_source": "FP64 pipe: 152 SMs x 4 flop/clk x 2070 MHz (nominal 1.25 TFLOP/s), above every "
+                              "measured probe rate"}
+        if calib:
+            out["fp64_probe_tflops"] = calib["fp64_gflops"] / 1e3
+            out["fp64_dmma_probe_tflops"] = calib.get("fp64_dmma_gflops", 0.0) / 1e3
+            out["fp64_probe_flop_per_clk_sm"] = calib.get("fp64_flop_per_clk_sm")
+            out["fp64_probe_sm_mhz"] = calib.get("fp64_sm_mhz")
         if clock_mhz:
             out["frac_at_sampled_clock"] = achieved / (peak * clock_mhz / NOMINAL_MAX_MHZ)
     return out
+
+
+def control_record(bs, torch, pb, ms, flush, stream, reps):
+    """The one-launch-per-triple control on the same plan and buffers."""
+    ctrl = lambda: bs.contract_uncoalesced(pb.P, pb.a, pb.b, pb.c, stream)  # noqa: E731
+    cms = statistics.median(time_steps(torch, ctrl, reps, 1 if reps > 1 else 0, flush, stream))
+    st = pb.stats
+    return {"ms": cms, "speedup": cms / ms, "launches_per_s": st["triples"] / (cms * 1e-3),
+            "gflops": st["useful_flops"] / (cms * 1e-3) / 1e9, "repeats": reps}
 
 
 def run_gpu(args):
@@ -222,6 +251,8 @@ def run_gpu(args):
     peaks = measured_peaks()
     calib = None if args.skip_calib else bs.calibrate(stream)
     log(f"[bench] calibration: {calib}")
+    if calib:
+        PLAN_OPTS.update(bs.calibrated_options(calib))
 
     w = bsgen.get(args.config)
     pb = Problem(bs, torch, w)
@@ -243,7 +274,8 @@ def run_gpu(args):
     value = weak_scaling_value(st["useful_flops"], world, ms) / 1e9
     blocks_s = weak_scaling_value(st["triples"], world, ms)
 
-    # end to end through the host-buffer entry point, pinned buffers
+    # end to end through the host-buffer entry point, pinned buffers: every call
+    # copies A and B in and C back and synchronizes
     a_pin = torch.from_numpy(pb.a_host).pin_memory()
     b_pin = torch.from_numpy(pb.b_host).pin_memory()
     c_pin = torch.zeros(pb.c.numel(), dtype=pb.c.dtype).pin_memory()
@@ -253,7 +285,8 @@ def run_gpu(args):
         t0 = time.perf_counter()
         bs.contract_host(pb.P, a_pin, b_pin, c_pin, stream)
         e2e_t.append(time.perf_counter() - t0)
-    e2e_s = statistics.mean(e2e_t)
+    e2e_s = max_over_ranks(statistics.mean(e2e_t), device="cuda")
+    del a_pin, b_pin, c_pin
 
     line = {
         "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -265,26 +298,33 @@ def run_gpu(args):
                    "useful_gflop": st["useful_flops"] / 1e9, "useful_mb": st["useful_bytes"] / 1e6,
                    "groups": st["groups"], "axis": ["auto", "contraction", "free", "none"][st["axis"]],
                    "packed": bool(st["packed_a"] or st["packed_b"]),
-                   "l2": "flushed before every step (256 MiB write, untimed)",
+                   "l2": "flushed before every step (256 MiB write, untimed)"
+                         + ("; inputs larger than L2" if st["useful_bytes"] > 129e6 else ""),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "gpu_launches": args.steps * st["launches"],
     }
-    kernel_ms = ms if st["launches"] == 1 else None
-    if kernel_ms is None:
-        kernel_ms = ms  # pack / zero fill share the step; reported as an upper bound on the kernel's time
+    # one bs_contract is one kernel when the plan neither gathers nor zero-fills,
+    # so the step time is that kernel's launch duration
+    kernel_ms = ms
     rl = roofline(w, st, kernel_ms, calib, peaks, clocks.get("sm_mhz"))
     tag = kernel_source_tag(w.dtype)
-    tr = recorded_traffic(w.name, tag)
-    rl["traffic"] = tr
+    rl["traffic"] = recorded_traffic(w.name, tag)
     rl["kernel"] = "bf16_grouped_kernel" if w.dtype == "bf16" else "fp64_grouped_kernel"
     rl["kernel_source"] = tag
+    rl["launches_per_step"] = st["launches"]
     line["roofline"] = rl
-    line["e2e"] = {"value": st["useful_flops"] / e2e_s / 1e9 * world, "unit": "GFLOP/s",
+    line["e2e"] = {"value": world * st["useful_flops"] / e2e_s / 1e9, "unit": "GFLOP/s",
                    "h2d_bytes_per_step": int(pb.a_host.nbytes + pb.b_host.nbytes),
-                   "d2h_bytes_per_step": int(c_pin.numel() * c_pin.element_size())}
+                   "d2h_bytes_per_step": int(pb.c.numel() * pb.c.element_size()),
+                   "ms_per_step": e2e_s * 1e3, "entry_point": "bs_contract_host (pinned host buffers)"}
     line["clocks"] = clocks
     line["calibration"] = calib
     line["model_us"] = st["model_us"]
+    line["model_over_measured"] = st["model_us"] / (ms * 1e3) if st["model_us"] else None
+    line["plan_ms"] = st["plan_ms"]
+    if not args.skip_control:
+        line["control"] = control_record(bs, torch, pb, ms, flush, stream, 1 if st["triples"] > 1e6 else 3)
+        log(f"[bench] control: {json.dumps(line['control'])}")
 
     if rank == 0 and world == 1 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_seconds, workers=args.cpu_workers)
@@ -301,6 +341,8 @@ def run_gpu(args):
 def per_config(bs, torch, flush, stream, calib, peaks, args, clock_mhz):
     out = {}
     for n in sorted(bsgen.CONFIGS):
+        if n == args.config:
+            continue
         w = bsgen.get(n)
         t0 = time.time()
         pb = Problem(bs, torch, w)
@@ -316,15 +358,13 @@ def per_config(bs, torch, flush, stream, calib, peaks, args, clock_mhz):
                "triples": st["triples"], "c_blocks": st["c_blocks"],
                "groups": st["groups"], "tasks": st["tasks"], "useful_gflop": st["useful_flops"] / 1e9,
                "useful_mb": st["useful_bytes"] / 1e6, "roofline_frac": rl["frac"], "roofline_bound": rl["bound"],
+               "roofline_achieved": rl["achieved"], "roofline_unit": rl["unit"], "roofline_peak": rl["peak"],
+               "traffic": recorded_traffic(w.name, kernel_source_tag(w.dtype)),
                "executed_over_useful": st["executed_flops"] / max(st["useful_flops"], 1),
-               "plan_ms": st["plan_ms"], "model_us": st["model_us"], "setup_s": setup_s}
-        if n in (1, 2) or (n == 5 and args.all_configs) or (n in (3, 4) and args.all_configs):
-            ctrl = lambda: bs.contract_uncoalesced(pb.P, pb.a, pb.b, pb.c, stream)  # noqa: E731
-            reps = 3 if n != 5 else 1
-            cms = statistics.median(time_steps(torch, ctrl, reps, 1, flush, stream))
-            rec["control_ms"] = cms
-            rec["speedup_vs_control"] = cms / ms
-            rec["control_launches_per_s"] = st["triples"] / (cms * 1e-3)
+               "plan_ms": st["plan_ms"], "model_us": st["model_us"],
+               "model_over_measured": st["model_us"] / (ms * 1e3) if st["model_us"] else None, "setup_s": setup_s}
+        if not args.skip_control:
+            rec["control"] = control_record(bs, torch, pb, ms, flush, stream, 3)
         out[str(n)] = rec
         log(f"[bench] config {n}: {json.dumps(rec)}")
         del pb
@@ -333,6 +373,38 @@ def per_config(bs, torch, flush, stream, calib, peaks, args, clock_mhz):
     log(f"[bench] chain: {json.dumps(out['chain'])}")
     out["bucket"] = bucket_record(bs, torch, flush, stream)
     log(f"[bench] bucket: {json.dumps(out['bucket'])}")
+    out["gather"] = gather_record(bs, torch, flush, stream, peaks)
+    log(f"[bench] gather: {json.dumps(out['gather'])}")
+    return out
+
+
+def gather_record(bs, torch, flush, stream, peaks):
+    """The gather ("pack") kernel on the pack-exercise layouts (every operand in
+    block-row order, gathered into charge-sorted panels), timed by the plan's own
+    phase events: bytes moved = 2 x packed bytes (each element read and written once)."""
+    hbm = peaks.get("hbm_gbs") or 6800.0
+    out = {}
+    for n, opts in ((5, dict(axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)), (4, {})):
+        w = bsgen.get(n)
+        w.layout_a, w.layout_b, w.layout_c = w.pack_layout_a, w.pack_layout_b, w.pack_layout_c
+        pb = Problem(bs, torch, w, profile=1, **opts)
+        g, k, tot = [], [], []
+        for _ in range(3 + 10):
+            flush.zero_()
+            bs.contract(pb.P, pb.a, pb.b, pb.c, stream)
+            pr = pb.P.profile()
+            g.append(pr["gather_ms"])
+            k.append(pr["kernel_ms"])
+            tot.append(pr["total_ms"])
+        assert bs.last_device_error(pb.P, stream) == 0
+        gm = statistics.median(g[3:])
+        gbs = pr["gather_bytes"] / (gm * 1e-3) / 1e9
+        out[str(n)] = {"workload": w.name + " (block-row operands)", "gather_ms": gm, "gather_bytes": pr["gather_bytes"],
+                       "gather_gbs": gbs, "gather_frac_of_hbm": gbs / hbm, "kernel_ms": statistics.median(k[3:]),
+                       "contract_ms": statistics.median(tot[3:]),
+                       "gflops": pb.stats["useful_flops"] / (statistics.median(tot[3:]) * 1e-3) / 1e9}
+        del pb
+        torch.cuda.empty_cache()
     return out
 
 
@@ -457,21 +529,9 @@ class OraclePool:
 
 
 def cpu_baseline(n: int, budget_s: float = 12.0, workers: int = 0):
-    """The oracle as it stands on the host cores, on the same workload: single-threaded,
-    and over every core (C blocks dealt longest-first over worker processes)."""
-    import oracle
-    w = bsgen.get(n)
-    pr = oracle.problem(w)
-    flops, _ = _workload_flops(w, pr)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.contract(pr)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s / 2 or (reps >= 1 and el * (reps + 1) / reps > budget_s):
-            break
-    single = {"value": flops * reps / el / 1e9, "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
-              "sample": f"the full {w.name} contraction, {reps} times in {el:.1f} s (plain C triple loop, FP64)"}
+    """The oracle as it stands on the host cores, on the same workload: over every
+    core (C blocks dealt longest-first over worker processes), the full contraction
+    per step; and single-threaded, on one worker's share of the C blocks."""
     pool = OraclePool(n, workers)
     try:
         pool.step()   # workers warm
@@ -482,9 +542,22 @@ def cpu_baseline(n: int, budget_s: float = 12.0, workers: int = 0):
             el = time.perf_counter() - t0
             if el >= budget_s / 2 or (reps >= 1 and el * (reps + 1) / reps > budget_s):
                 break
+        # one core: the first worker's share, run in this process
+        import oracle
+        w = bsgen.get(n)
+        pr = oracle.problem(w)
+        share = pool.parts[0]
+        sfl = sum(2.0 * float(w.rows.d[i]) * float(w.cols.d[j]) *
+                  float(w.inner.d[np.nonzero(pr.ma[i] * pr.mb[:, j])[0]].sum()) for i, j in share)
+        t1 = time.perf_counter()
+        oracle.contract(pr, sel=share)
+        el1 = time.perf_counter() - t1
     finally:
         pool.close()
-    return {"value": flops * reps / el / 1e9, "unit": "GFLOP/s", "cores": pool.workers, "kind": "oracle",
+    single = {"value": sfl / el1 / 1e9, "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+              "sample": f"{len(share)} of the {w.name} C blocks ({sfl / pool.flops:.1%} of its flops) in {el1:.1f} s "
+                        f"(plain C triple loop, FP64)"}
+    return {"value": pool.flops * reps / el / 1e9, "unit": "GFLOP/s", "cores": pool.workers, "kind": "oracle",
             "sample": f"the full {w.name} contraction, {reps} times in {el:.1f} s, its C blocks dealt over "
                       f"{pool.workers} worker processes on {cpu_model()}",
             "single_core": single}
@@ -527,9 +600,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", type=int, default=2, choices=sorted(bsgen.CONFIGS))
-    ap.add_argument("--all-configs", action="store_true", help="also time the control on configs 3-5")
+    ap.add_argument("--config", type=int, default=5, choices=sorted(bsgen.CONFIGS))
     ap.add_argument("--skip-configs", action="store_true", help="headline workload only")
+    ap.add_argument("--skip-control", action="store_true", help="skip the one-launch-per-triple controls")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-workers", type=int, default=0, help="oracle worker processes (0: every core)")

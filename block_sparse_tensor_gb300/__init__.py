@@ -34,7 +34,8 @@ EXPORTED = ["bs_layout_create", "bs_layout_query", "bs_layout_blocks", "bs_layou
             "bs_plan_groups", "bs_plan_triples", "bs_contract", "bs_contract_host",
             "bs_contract_uncoalesced", "bs_plan_last_device_error", "bs_plan_destroy",
             "bs_status_string", "bs_version", "bs_calibrate", "bs_contract_noalloc",
-            "bs_plan_check_groups", "bs_plan_create_into"]
+            "bs_plan_check_groups", "bs_plan_create_into", "bs_plan_profile", "bs_plan_create_shard",
+            "bs_plan_operand_blocks", "bs_calibration_apply"]
 
 
 class BsError(RuntimeError):
@@ -65,7 +66,11 @@ class PlanOptions(ctypes.Structure):
                 ("t_segment_us", ctypes.c_double), ("pack_gbs", ctypes.c_double),
                 ("fp64_gflops", ctypes.c_double), ("atomic_penalty", ctypes.c_double),
                 ("wait_timeout_ms", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
-                ("bucket_pad", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+                ("bucket_pad", ctypes.c_int32), ("profile", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4),
+                ("t_fixed_us", ctypes.c_double), ("fp64_tail_gflops", ctypes.c_double),
+                ("fp64_general_gflops", ctypes.c_double), ("pack_fixed_us", ctypes.c_double),
+                ("zero_gbs", ctypes.c_double), ("bf16_stage_us", ctypes.c_double), ("bf16_tile_us", ctypes.c_double),
+                ("reserved2", ctypes.c_double * 4)]
 
 
 class PlanStats(ctypes.Structure):
@@ -78,10 +83,20 @@ class PlanStats(ctypes.Structure):
                 ("model_us", ctypes.c_double), ("model_us_alt", ctypes.c_double), ("plan_ms", ctypes.c_double)]
 
 
+class PhaseTimes(ctypes.Structure):
+    _fields_ = [("gather_ms", ctypes.c_double), ("zero_ms", ctypes.c_double), ("kernel_ms", ctypes.c_double),
+                ("total_ms", ctypes.c_double), ("gather_bytes", ctypes.c_int64), ("reserved", ctypes.c_int64 * 3)]
+
+
 class Calibration(ctypes.Structure):
     _fields_ = [("fp64_gflops", ctypes.c_double), ("fp64_gflops_quarter_warp", ctypes.c_double),
                 ("launch_us", ctypes.c_double), ("copy_gbs", ctypes.c_double), ("sm_count", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 7)]
+                ("sm_id_bound", ctypes.c_int32), ("fp64_sm_mhz", ctypes.c_double),
+                ("fp64_flop_per_clk_sm", ctypes.c_double), ("fp64_dmma_gflops", ctypes.c_double),
+                ("dmma_flop_per_clk_sm", ctypes.c_double), ("t_fixed_us", ctypes.c_double),
+                ("tile_gflops", ctypes.c_double), ("tail_gflops", ctypes.c_double), ("general_gflops", ctypes.c_double),
+                ("pack_gbs", ctypes.c_double), ("pack_fixed_us", ctypes.c_double), ("zero_gbs", ctypes.c_double),
+                ("bf16_stage_us", ctypes.c_double), ("bf16_tile_us", ctypes.c_double), ("reserved", ctypes.c_double * 7)]
 
 
 def _load(path: str = LIB_PATH):
@@ -112,6 +127,10 @@ def _load(path: str = LIB_PATH):
         "bs_contract_noalloc": (st, [P, P, P, P, P]),
         "bs_plan_check_groups": (st, [P, P]),
         "bs_plan_create_into": (st, [P, P, P, i32, P, P]),
+        "bs_plan_profile": (st, [P, P]),
+        "bs_plan_create_shard": (st, [P, P, i32, P, i32, i32, P]),
+        "bs_plan_operand_blocks": (st, [P, i32, P, P]),
+        "bs_calibration_apply": (None, [P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -244,11 +263,15 @@ def plan_options(**kw) -> PlanOptions:
 class Plan:
     """A contraction plan (bs_plan) for C = A B."""
 
-    def __init__(self, A: Layout, B: Layout, dtype: int = F64, C: Layout = None, **options):
-        """With C, plan onto that existing C layout (bs_plan_create_into)."""
+    def __init__(self, A: Layout, B: Layout, dtype: int = F64, C: Layout = None, shard=None, **options):
+        """With C, plan onto that existing C layout (bs_plan_create_into); with
+        shard = (rank, world), plan shard `rank` of `world` (bs_plan_create_shard)."""
         self.opts = plan_options(**options)
         h = ctypes.c_void_p()
-        if C is None:
+        if shard is not None:
+            _check(lib.bs_plan_create_shard(A.h, B.h, int(dtype), ctypes.byref(self.opts), int(shard[0]), int(shard[1]),
+                                            ctypes.byref(h)), "bs_plan_create_shard")
+        elif C is None:
             _check(lib.bs_plan_create(A.h, B.h, int(dtype), ctypes.byref(self.opts), ctypes.byref(h)), "bs_plan_create")
         else:
             _check(lib.bs_plan_create_into(A.h, B.h, C.h, int(dtype), ctypes.byref(self.opts), ctypes.byref(h)),
@@ -284,6 +307,21 @@ class Plan:
         _check(lib.bs_plan_triples(self.h, ctypes.byref(nt), ctypes.byref(ng), ptr.ctypes.data, tr.ctypes.data),
                "bs_plan_triples")
         return ptr, tr[:nt.value]
+
+    def operand_blocks(self, operand: int) -> np.ndarray:
+        """Indices (storage order) of the A (0), B (1) or C (2) blocks this plan uses."""
+        n = ctypes.c_int64()
+        _check(lib.bs_plan_operand_blocks(self.h, int(operand), ctypes.byref(n), None), "bs_plan_operand_blocks")
+        out = np.zeros(max(n.value, 1), np.int32)
+        _check(lib.bs_plan_operand_blocks(self.h, int(operand), ctypes.byref(n), out.ctypes.data),
+               "bs_plan_operand_blocks")
+        return out[:n.value]
+
+    def profile(self) -> dict:
+        """Phase times (ms) of the last contraction of a plan built with profile=1."""
+        t = PhaseTimes()
+        _check(lib.bs_plan_profile(self.h, ctypes.byref(t)), "bs_plan_profile")
+        return {name: getattr(t, name) for name, _ in PhaseTimes._fields_ if name != "reserved"}
 
     def __del__(self):
         if getattr(self, "h", None):
@@ -325,7 +363,20 @@ def calibrate(stream=None) -> dict:
     """Measure the cost-model constants on the current device (bs_calibrate)."""
     c = Calibration()
     _check(lib.bs_calibrate(ctypes.byref(c), _stream(stream)), "bs_calibrate")
-    return {name: getattr(c, name) for name, _ in Calibration._fields_ if name != "reserved"}
+    return {name: getattr(c, name) for name, _ in Calibration._fields_ if not name.startswith("reserved")}
+
+
+def calibrated_options(cal: dict) -> dict:
+    """Planner options carrying the cost-model constants of a calibration (bs_calibration_apply)."""
+    c = Calibration()
+    for name, _ in Calibration._fields_:
+        if not name.startswith("reserved") and name in cal:
+            setattr(c, name, cal[name])
+    o = plan_options()
+    lib.bs_calibration_apply(ctypes.byref(c), ctypes.byref(o))
+    names = ("t_launch_us", "t_task_us", "t_segment_us", "pack_gbs", "fp64_gflops", "atomic_penalty", "t_fixed_us",
+             "fp64_tail_gflops", "fp64_general_gflops", "pack_fixed_us", "zero_gbs", "bf16_stage_us", "bf16_tile_us")
+    return {n: getattr(o, n) for n in names if getattr(o, n) > 0}
 
 
 def version() -> str:

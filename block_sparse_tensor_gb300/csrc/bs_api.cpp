@@ -33,6 +33,15 @@ bs_status cuda_status(cudaError_t e) {
     if (e_ != cudaSuccess) return cuda_status(e_);           \
   } while (0)
 
+// Host allocation fault injection for tests: with BS_FAULT_INJECT=alloc in the
+// environment, the allocations of layout and plan construction fail (as if the
+// host were out of memory), so the error path and its clean-up can be
+// exercised without exhausting anything.  Nothing on the device is involved.
+bool alloc_fault_injected() {
+  const char *v = std::getenv("BS_FAULT_INJECT");
+  return v && std::strstr(v, "alloc") != nullptr;
+}
+
 Sparsity sparsity_of(const bs_layout &L) {
   Sparsity sp;
   sp.ptr.assign(L.rows.n + 1, 0);
@@ -79,12 +88,15 @@ int64_t populated_elems(const bs_layout &L) {
   return s;
 }
 
-// Block copies of the gather, split into row bands of at most 16K elements so
-// one huge block does not serialise the launch on a single CTA.
+// Block copies of the gather (one warp each), split into row bands of at most
+// 2048 elements so one huge block does not serialise the launch on a few
+// warps, and listed largest first so the warps that take them in turn get
+// equal shares.
 void pack_list(const bs_layout &src, const bs_layout &dst, std::vector<PackCopy> *out) {
+  const size_t first = out->size();
   for (const auto &b : src.blocks) {
     const auto &d = dst.blocks[dst.find(b.row, b.col)];
-    const int32_t band = std::max<int32_t>(1, 16384 / b.cols);
+    const int32_t band = std::max<int32_t>(1, 2048 / b.cols);
     for (int32_t r0 = 0; r0 < b.rows; r0 += band) {
       PackCopy c{};
       c.src = b.offset + (int64_t)r0 * b.ld;
@@ -96,10 +108,15 @@ void pack_list(const bs_layout &src, const bs_layout &dst, std::vector<PackCopy>
       out->push_back(c);
     }
   }
+  std::stable_sort(out->begin() + first, out->end(), [](const PackCopy &x, const PackCopy &y) {
+    return (int64_t)x.rows * x.cols > (int64_t)y.rows * y.cols;
+  });
 }
 
-void zero_list(const bs_layout &C, std::vector<ZeroBlock> *out) {
-  for (const auto &b : C.blocks) {
+void zero_list(const bs_layout &C, const std::vector<uint8_t> *cmask, std::vector<ZeroBlock> *out) {
+  for (size_t t = 0; t < C.blocks.size(); ++t) {
+    if (cmask && !(*cmask)[t]) continue;   // another shard's C block
+    const auto &b = C.blocks[t];
     const int32_t band = std::max<int32_t>(1, 16384 / b.cols);
     for (int32_t r0 = 0; r0 < b.rows; r0 += band)
       out->push_back({b.offset + (int64_t)r0 * b.ld, b.ld, std::min(band, b.rows - r0), b.cols});
@@ -261,8 +278,6 @@ bs_status upload(bs_plan *P) {
   size_t o_ksegs = append_bytes(buf, P->gs.ksegs);
   size_t o_tail = append_bytes(buf, P->ts.tail_elems);
   size_t o_tdesc = append_bytes(buf, P->ts.tdesc);
-  size_t o_tqp = append_bytes(buf, P->ts.tq_ptr);
-  size_t o_tqi = append_bytes(buf, P->ts.tq_items);
   size_t o_pack = append_bytes(buf, P->pack_copies);
   size_t o_zero = append_bytes(buf, P->zero_blocks);
   size_t o_bc = append_bytes(buf, P->bctas);
@@ -282,8 +297,6 @@ bs_status upload(bs_plan *P) {
   P->d_ksegs = (KSeg *)(b + o_ksegs);
   P->d_tail = (int32_t *)(b + o_tail);
   P->d_tdesc = (TailDesc *)(b + o_tdesc);
-  P->d_tq_ptr = (int32_t *)(b + o_tqp);
-  P->d_tq_items = (int32_t *)(b + o_tqi);
   P->d_pack = (PackCopy *)(b + o_pack);
   P->d_zero = (ZeroBlock *)(b + o_zero);
   P->d_bctas = (Bf16Cta *)(b + o_bc);
@@ -306,6 +319,11 @@ bs_status upload(bs_plan *P) {
 }
 
 void free_device(bs_plan *P) {
+  for (auto &e : P->ev)
+    if (e) {
+      cudaEventDestroy(e);
+      e = nullptr;
+    }
   cudaFree(P->d_tables);
   cudaFree(P->d_counter);
   cudaFree(P->d_ws_a);
@@ -324,6 +342,8 @@ struct Candidate {
 };
 
 }  // namespace
+
+static bs_status contract_kernel(bs_plan *P, const void *Ause, const void *Buse, void *C, cudaStream_t s);
 
 extern "C" {
 
@@ -354,6 +374,10 @@ bs_status bs_layout_create(const bs_axis_desc *rows, const bs_axis_desc *cols, c
   if (rule->dq_min > rule->dq_max) return BS_ERR_INVALID_ARG;
   bs_layout *L = new (std::nothrow) bs_layout();
   if (!L) return BS_ERR_OOM;
+  if (alloc_fault_injected()) {
+    delete L;
+    return BS_ERR_OOM;
+  }
   AxisCopy r, c;
   bs_status st = copy_axis(rows, &r);
   if (st == BS_OK) st = copy_axis(cols, &c);
@@ -398,10 +422,11 @@ void bs_plan_options_default(bs_plan_options *o) {
 }
 
 static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_layout *Cg, int32_t dtype,
-                             const bs_plan_options *opts, bs_plan **out) {
+                             const bs_plan_options *opts, bs_plan **out, int32_t rank = 0, int32_t world = 1) {
   if (!out) return BS_ERR_INVALID_ARG;
   *out = nullptr;
   if (!A || !B) return BS_ERR_INVALID_ARG;
+  if (world < 1 || rank < 0 || rank >= world) return BS_ERR_INVALID_ARG;
   if (dtype != BS_F64 && dtype != BS_BF16_F32) return BS_ERR_INVALID_ARG;
   bs_plan_options o;
   bs_plan_options_default(&o);
@@ -423,6 +448,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
   try {
     P->dtype = dtype;
     P->opts = o;
+    if (alloc_fault_injected()) throw std::bad_alloc();   // taken by the OOM path below
     P->A = *A;
     P->B = *B;
     if (Cg) {
@@ -452,6 +478,13 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
       delete P;
       return st;
     }
+    // a shard computes only its C blocks; C's layout stays the whole product
+    if (world > 1) {
+      P->cmask = shard_mask(*A, *B, P->C, rank, world);
+      P->shard_rank = rank;
+      P->shard_world = world;
+    }
+    const std::vector<uint8_t> *cm = world > 1 ? &P->cmask : nullptr;
     PlanModel pm;
     if (o.t_launch_us > 0) pm.t_launch_us = o.t_launch_us;
     if (o.t_task_us > 0) pm.t_task_us = o.t_task_us;
@@ -459,7 +492,14 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
     if (o.pack_gbs > 0) pm.pack_gbs = o.pack_gbs;
     if (o.fp64_gflops > 0) pm.fp64_gflops = o.fp64_gflops;
     if (o.atomic_penalty > 0) pm.atomic_penalty = o.atomic_penalty;
-    if (o.bucket_pad < 0 || o.bucket_pad > 1) {
+    if (o.t_fixed_us > 0) pm.t_fixed_us = o.t_fixed_us;
+    if (o.fp64_tail_gflops > 0) pm.tail_gflops = o.fp64_tail_gflops;
+    if (o.fp64_general_gflops > 0) pm.general_gflops = o.fp64_general_gflops;
+    if (o.pack_fixed_us > 0) pm.pack_fixed_us = o.pack_fixed_us;
+    if (o.zero_gbs > 0) pm.zero_gbs = o.zero_gbs;
+    if (o.bf16_stage_us > 0) pm.bf16_stage_us = o.bf16_stage_us;
+    if (o.bf16_tile_us > 0) pm.bf16_tile_us = o.bf16_tile_us;
+    if (o.bucket_pad < 0 || o.bucket_pad > 1 || o.profile < 0 || o.profile > 1) {
       delete P;
       return BS_ERR_INVALID_ARG;
     }
@@ -479,9 +519,22 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
       P->device = dev;
       cudaDeviceGetAttribute(&P->sm_count, cudaDevAttrMultiProcessorCount, dev);
     } else {
-      P->sm_count = 152;
+      // a host-only plan follows the current device when there is one (so the
+      // allocation-free entry point launches the grid the plan was dealt for),
+      // else a 152-SM part
+      int dev = 0, sms = 0;
+      if (cudaGetDevice(&dev) == cudaSuccess &&
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+        P->sm_count = sms;
+        P->device = dev;
+      } else {
+        (void)cudaGetLastError();
+        P->sm_count = 152;
+      }
     }
-    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : (o.host_only ? 3 : std::max(1, fp64_max_ctas_per_sm(false)));
+    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm
+                    : (o.host_only && P->device < 0) ? 3
+                                                      : std::max(1, fp64_max_ctas_per_sm(false));
     pm.parallel_ctas = P->sm_count * cps;
     pm.sms = P->sm_count;
 
@@ -540,15 +593,19 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
           }
         }
         const auto tg0 = std::chrono::steady_clock::now();
-        c.gs = ax == BS_AXIS_CONTRACTION ? make_contraction_groups(*Ae, *Be, P->C, o.merge_rows != 0, false, unchecked)
-               : ax == BS_AXIS_FREE      ? make_free_groups(*Ae, *Be, P->C)
-                                         : make_triple_groups(*Ae, *Be, P->C);
+        c.gs = ax == BS_AXIS_CONTRACTION ? make_contraction_groups(*Ae, *Be, P->C, o.merge_rows != 0, false, unchecked, cm)
+               : ax == BS_AXIS_FREE      ? make_free_groups(*Ae, *Be, P->C, cm)
+                                         : make_triple_groups(*Ae, *Be, P->C, cm);
         const auto tg1 = std::chrono::steady_clock::now();
         tile_fp64(c.gs, pm, &c.ts, only);
         const auto tg2 = std::chrono::steady_clock::now();
         const bool atomic = ax != BS_AXIS_CONTRACTION;
         const int launches = 1 + (pk ? 1 : 0) + (atomic ? 1 : 0);
-        c.us = model_fp64_us(c.gs, c.ts, pm, pbytes, launches);
+        int64_t zbytes = 0;   // C blocks of this plan, zero-filled before atomic scatter
+        if (atomic)
+          for (size_t t = 0; t < P->C.blocks.size(); ++t)
+            if (!cm || P->cmask[t]) zbytes += (int64_t)P->C.blocks[t].rows * P->C.blocks[t].cols * 8;
+        c.us = model_fp64_us(c.gs, c.ts, pm, pbytes, launches, zbytes);
         c.ms_group = std::chrono::duration<double, std::milli>(tg1 - tg0).count();
         c.ms_tile = std::chrono::duration<double, std::milli>(tg2 - tg1).count();
       };
@@ -593,6 +650,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
         delete P;
         return st;
       }
+      std::vector<Built>().swap(built);   // the losing candidates go before the winner is listed in full
       if (!only) tile_fp64(P->gs, pm, &P->ts, true);   // the chosen candidate in full
       P->axis = best_axis;
       P->stats.model_us = best;
@@ -603,7 +661,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
       (void)best_pack;
     } else {
       // BF16: contraction axis; views must satisfy the tensor-map rules, else gather
-      GroupSet gs = make_contraction_groups(P->A, P->B, P->C, o.merge_rows != 0, false, unchecked);
+      GroupSet gs = make_contraction_groups(P->A, P->B, P->C, o.merge_rows != 0, false, unchecked, cm);
       bool need_pack = !groups_tma_ok(gs) || o.pack_policy == BS_PACK_ALWAYS;
       if (need_pack && o.pack_policy == BS_PACK_NEVER) {
         delete P;
@@ -617,7 +675,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
           return st;
         }
         P->pack_a = P->pack_b = true;
-        gs = make_contraction_groups(P->A_pk, P->B_pk, P->C, o.merge_rows != 0, false, unchecked);
+        gs = make_contraction_groups(P->A_pk, P->B_pk, P->C, o.merge_rows != 0, false, unchecked, cm);
       }
       P->gs = std::move(gs);
       P->axis = BS_AXIS_CONTRACTION;
@@ -628,7 +686,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
     if (P->pack_b) pack_list(P->B, P->B_pk, &P->pack_copies);
     bool any_atomic = false;
     for (const auto &g : P->gs.groups) any_atomic |= (g.flags & GF_ATOMIC) != 0;
-    if (any_atomic) zero_list(P->C, &P->zero_blocks);
+    if (any_atomic) zero_list(P->C, cm, &P->zero_blocks);
 
     // statistics
     bs_plan_stats &S = P->stats;
@@ -640,7 +698,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
     for (size_t t = 0; t < tr.size(); t += 3)
       fl += 2.0 * A->rows.d[tr[t]] * A->cols.d[tr[t + 1]] * B->cols.d[tr[t + 2]];
     S.useful_flops = fl;
-    S.c_blocks = (int64_t)P->C.blocks.size();
+    S.c_blocks = cm ? (int64_t)std::count(P->cmask.begin(), P->cmask.end(), (uint8_t)1) : (int64_t)P->C.blocks.size();
     S.groups = (int64_t)P->gs.groups.size();
     int64_t nseg = 0;
     for (const auto &g : P->gs.groups) nseg += std::max(g.kseg_count, g.rseg_count);
@@ -650,7 +708,21 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
     S.packed_b = P->pack_b;
     S.packed_bytes = (P->pack_a ? populated_elems(P->A) * eb_in : 0) + (P->pack_b ? populated_elems(P->B) * eb_in : 0);
     const int eb_out = dtype == BS_F64 ? 8 : 4;
-    S.useful_bytes = (double)(populated_elems(P->A) + populated_elems(P->B)) * eb_in + (double)populated_elems(P->C) * eb_out;
+    if (!cm) {
+      S.useful_bytes = (double)(populated_elems(P->A) + populated_elems(P->B)) * eb_in + (double)populated_elems(P->C) * eb_out;
+    } else {   // the blocks this shard reads and writes
+      std::vector<uint8_t> ua(P->A.blocks.size(), 0), ub(P->B.blocks.size(), 0);
+      double by = 0;
+      for (size_t t = 0; t < tr.size(); t += 3) {
+        const int32_t a = P->A.find(tr[t], tr[t + 1]), b = P->B.find(tr[t + 1], tr[t + 2]);
+        if (!ua[a]) by += (double)P->A.blocks[a].rows * P->A.blocks[a].cols * eb_in;
+        if (!ub[b]) by += (double)P->B.blocks[b].rows * P->B.blocks[b].cols * eb_in;
+        ua[a] = ub[b] = 1;
+      }
+      for (size_t t = 0; t < P->C.blocks.size(); ++t)
+        if (P->cmask[t]) by += (double)P->C.blocks[t].rows * P->C.blocks[t].cols * eb_out;
+      S.useful_bytes = by;
+    }
     if (dtype == BS_F64) {
       S.tile_tasks = (int64_t)P->ts.tasks.size();
       S.tail_tasks = (int64_t)(P->ts.tail_elems.size() / 2 + kThreads - 1) / kThreads;   // CTA-sized pieces of the tail list
@@ -667,8 +739,16 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
       S.executed_flops = ex;
     }
     S.launches = 1 + ((P->pack_a || P->pack_b) ? 1 : 0) + (P->zero_blocks.empty() ? 0 : 1);
+    if (dtype == BS_BF16_F32) S.model_us = model_bf16_us(*P, pm);
 
     if (!o.host_only) {
+      if (dtype == BS_F64 && P->ts.tq_ptr.size() > 1) {
+        st = sm_index_map(P->device, P->sm_count, nullptr, 0, &P->sm_map);
+        if (st != BS_OK) {
+          delete P;
+          return st;
+        }
+      }
       st = upload(P);
       if (st != BS_OK) {
         free_device(P);
@@ -695,6 +775,50 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
 bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype, const bs_plan_options *opts,
                          bs_plan **out) {
   return plan_create(A, B, nullptr, dtype, opts, out);
+}
+
+void bs_calibration_apply(const bs_calibration *c, bs_plan_options *o) {
+  if (!c || !o) return;
+  auto set = [](double v, double *dst) {
+    if (v > 0) *dst = v;
+  };
+  set(c->t_fixed_us, &o->t_fixed_us);
+  set(c->launch_us, &o->t_launch_us);
+  set(c->tile_gflops, &o->fp64_gflops);
+  set(c->tail_gflops, &o->fp64_tail_gflops);
+  set(c->general_gflops, &o->fp64_general_gflops);
+  set(c->pack_gbs, &o->pack_gbs);
+  set(c->pack_fixed_us, &o->pack_fixed_us);
+  set(c->zero_gbs, &o->zero_gbs);
+  set(c->bf16_stage_us, &o->bf16_stage_us);
+  set(c->bf16_tile_us, &o->bf16_tile_us);
+}
+
+bs_status bs_plan_create_shard(const bs_layout *A, const bs_layout *B, int32_t dtype, const bs_plan_options *opts,
+                               int32_t rank, int32_t world, bs_plan **out) {
+  return plan_create(A, B, nullptr, dtype, opts, out, rank, world);
+}
+
+bs_status bs_plan_operand_blocks(const bs_plan *P, int32_t operand, int64_t *n, int32_t *out) {
+  if (!P || !n || operand < 0 || operand > 2) return BS_ERR_INVALID_ARG;
+  const bs_layout &L = operand == 0 ? P->A : operand == 1 ? P->B : P->C;
+  std::vector<uint8_t> used(L.blocks.size(), 0);
+  std::vector<int64_t> tp;
+  std::vector<int32_t> tr;
+  group_triples(P->gs, &tp, &tr);
+  for (size_t t = 0; t < tr.size(); t += 3) {
+    const int32_t r = operand == 1 ? tr[t + 1] : tr[t];
+    const int32_t c = operand == 0 ? tr[t + 1] : tr[t + 2];
+    used[L.find(r, c)] = 1;
+  }
+  int64_t cnt = 0;
+  for (size_t b = 0; b < used.size(); ++b)
+    if (used[b]) {
+      if (out) out[cnt] = (int32_t)b;
+      ++cnt;
+    }
+  *n = cnt;
+  return BS_OK;
 }
 
 bs_status bs_plan_create_into(const bs_layout *A, const bs_layout *B, const bs_layout *C, int32_t dtype,
@@ -858,6 +982,12 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
   cudaStream_t s = (cudaStream_t)stream;
   const void *Ause = P->pack_a ? P->d_ws_a : A;
   const void *Buse = P->pack_b ? P->d_ws_b : B;
+  const bool prof = P->opts.profile != 0;
+  if (prof) {
+    for (auto &e : P->ev)
+      if (!e) BS_CUDA(cudaEventCreate(&e));
+    BS_CUDA(cudaEventRecord(P->ev[0], s));
+  }
   if (!P->pack_copies.empty()) {
     PackParams pp{};
     pp.src = A;
@@ -869,10 +999,23 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
     PackParams pb = pp;
     pb.src = B;
     pb.dst = P->d_ws_b;
-    BS_CUDA(launch_pack2(pp, pb, (int32_t)P->pack_copies.size(), P->sm_count * 4, s));
+    BS_CUDA(launch_pack2(pp, pb, (int32_t)P->pack_copies.size(), P->sm_count * 8, s));
   }
+  if (prof) BS_CUDA(cudaEventRecord(P->ev[1], s));
   if (!P->zero_blocks.empty())
     BS_CUDA(launch_zero(C, P->dtype == BS_F64 ? 8 : 4, P->d_zero, (int)P->zero_blocks.size(), P->sm_count * 4, s));
+  if (prof) BS_CUDA(cudaEventRecord(P->ev[2], s));
+  bs_status st = contract_kernel(P, Ause, Buse, C, s);
+  if (st == BS_OK && prof) {
+    BS_CUDA(cudaEventRecord(P->ev[3], s));
+    P->ev_recorded = true;
+  }
+  return st;
+}
+
+}  // extern "C"
+
+static bs_status contract_kernel(bs_plan *P, const void *Ause, const void *Buse, void *C, cudaStream_t s) {
   if (P->dtype == BS_F64) {
     if (P->ts.tasks.empty() && P->ts.tail_elems.empty()) return BS_OK;
     Fp64Params p{};
@@ -888,9 +1031,7 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
     p.ntasks = (int32_t)P->ts.tasks.size();
     p.ntail = (int32_t)(P->ts.tail_elems.size() / 2);
     p.nct = (int32_t)((p.ntail + kThreads - 1) / kThreads);
-    p.nq = (int32_t)P->ts.tq_ptr.size() - 1;
-    p.tq_ptr = P->d_tq_ptr;
-    p.tq_items = P->d_tq_items;
+    fill_queue_params(&p, P->ts.tq_ptr, P->sm_map);
     p.counter = P->d_counter;
     p.status = P->d_status;
     BS_CUDA(launch_fp64_grouped(p, P->grid, s));
@@ -917,6 +1058,22 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
     p.debug_flags = P->opts.debug_flags;
     BS_CUDA(launch_bf16_grouped(p, P->grid, s));
   }
+  return BS_OK;
+}
+
+extern "C" {
+
+bs_status bs_plan_profile(bs_plan *P, bs_phase_times *out) {
+  if (!P || !out || P->opts.host_only || !P->opts.profile || !P->ev_recorded) return BS_ERR_INVALID_ARG;
+  *out = bs_phase_times{};
+  BS_CUDA(cudaEventSynchronize(P->ev[3]));
+  float t[3] = {0, 0, 0};
+  for (int i = 0; i < 3; ++i) BS_CUDA(cudaEventElapsedTime(&t[i], P->ev[i], P->ev[i + 1]));
+  out->gather_ms = P->pack_copies.empty() ? 0.0 : t[0];
+  out->zero_ms = P->zero_blocks.empty() ? 0.0 : t[1];
+  out->kernel_ms = t[2];
+  out->total_ms = (double)t[0] + t[1] + t[2];
+  out->gather_bytes = 2 * P->stats.packed_bytes;
   return BS_OK;
 }
 

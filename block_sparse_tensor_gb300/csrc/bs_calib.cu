@@ -11,9 +11,12 @@
 //   - the bandwidth of a plain device-to-device copy kernel (the gather).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <chrono>
+#include <cmath>
+#include <vector>
 
-#include "bs_host.h"
+#include "bs_plan.h"
 
 namespace bs {
 
@@ -21,27 +24,76 @@ namespace {
 
 constexpr int kFmaIters = 4096;
 
-// Eight independent FMA chains per thread keep the pipe busy; `active`
-// lanes of each warp do the work, the others skip it.
-__global__ void dfma_probe(double *out, double seed, int active) {
+// Clock record of one CTA: SM cycles and global time at its start and end.
+struct ClockRec {
+  long long c0, c1;
+  unsigned long long t0, t1;
+};
+
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// C independent FMA chains per thread keep the pipe busy; `active` lanes of
+// each warp do the work, the others skip it.  Thread 0 records its CTA's SM
+// cycles and global time, which give the SM clock during the probe.
+template <int C>
+__global__ void dfma_probe(double *out, ClockRec *rec, double seed, int active) {
+  const long long c0 = clock64();
+  const unsigned long long t0 = gtimer();
   const int lane = threadIdx.x & 31;
-  if (lane >= active) return;
-  double a0 = seed + threadIdx.x, a1 = a0 + 1, a2 = a0 + 2, a3 = a0 + 3, a4 = a0 + 4, a5 = a0 + 5, a6 = a0 + 6,
-         a7 = a0 + 7;
-  const double m = 0.999999, c = 1e-7;
-#pragma unroll 4
-  for (int i = 0; i < kFmaIters; ++i) {
-    a0 = fma(a0, m, c);
-    a1 = fma(a1, m, c);
-    a2 = fma(a2, m, c);
-    a3 = fma(a3, m, c);
-    a4 = fma(a4, m, c);
-    a5 = fma(a5, m, c);
-    a6 = fma(a6, m, c);
-    a7 = fma(a7, m, c);
+  if (lane < active) {
+    // every chain has its own operand registers: acc += x * y, as in a GEMM
+    double a[C], x[C], y[C];
+#pragma unroll
+    for (int u = 0; u < C; ++u) {
+      a[u] = seed + threadIdx.x + u;
+      x[u] = 1e-3 * (u + 1);
+      y[u] = 1e-3 * (seed + u);
+    }
+#pragma unroll 2
+    for (int i = 0; i < kFmaIters; ++i) {
+#pragma unroll
+      for (int u = 0; u < C; ++u) a[u] = fma(x[u], y[u], a[u]);
+    }
+    double s = 0.0;
+#pragma unroll
+    for (int u = 0; u < C; ++u) s += a[u];
+    if (s == 12345.678) out[blockIdx.x * blockDim.x + threadIdx.x] = s;   // keeps the loop alive
   }
-  const double s = a0 + a1 + a2 + a3 + a4 + a5 + a6 + a7;
-  if (s == 12345.678) out[blockIdx.x * blockDim.x + threadIdx.x] = s;   // keeps the loop alive
+  __syncthreads();
+  if (threadIdx.x == 0 && rec) rec[blockIdx.x] = {c0, clock64(), t0, gtimer()};
+}
+
+// The FP64 matrix instruction (mma.sync m8n8k4, 512 flops per warp
+// instruction) with eight independent accumulator pairs per warp.
+__global__ void dmma_probe(double *out, ClockRec *rec, double seed) {
+  const long long c0 = clock64();
+  const unsigned long long t0 = gtimer();
+  double a[8], b[8], d[16];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    a[u] = 1e-3 * (u + 1) + seed * 1e-9 * threadIdx.x;
+    b[u] = 1e-3 * (8 - u);
+  }
+#pragma unroll
+  for (int u = 0; u < 16; ++u) d[u] = 0.0;
+#pragma unroll 1
+  for (int i = 0; i < kFmaIters / 4; ++i) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      asm volatile("mma.sync.aligned.m8n8k4.row.col.f64.f64.f64.f64 {%0, %1}, {%2}, {%3}, {%0, %1};"
+                   : "+d"(d[2 * u]), "+d"(d[2 * u + 1])
+                   : "d"(a[u]), "d"(b[u]));
+  }
+  double s = 0.0;
+#pragma unroll
+  for (int u = 0; u < 16; ++u) s += d[u];
+  if (s == 12345.678) out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.x == 0 && rec) rec[blockIdx.x] = {c0, clock64(), t0, gtimer()};
 }
 
 __global__ void empty_kernel() {}
@@ -51,6 +103,204 @@ __global__ void copy_probe(const double4_32a *src, double4_32a *dst, size_t n) {
     dst[i] = src[i];
 }
 
+// ---- cost-model constants from the library's own kernels ------------------
+
+// One synthetic structure: three axes of band sectors (rule |dq| <= band on
+// both operands), layouts, plan options.
+struct CalStruct {
+  std::vector<int32_t> q[3], d[3];
+  int32_t band = 1;
+  uint32_t flags[3] = {BS_LAYOUT_ROWPANEL | BS_LAYOUT_CHARGE_SORTED, BS_LAYOUT_COLPANEL | BS_LAYOUT_CHARGE_SORTED,
+                       BS_LAYOUT_BLOCKROW};
+  int32_t dtype = BS_F64;
+};
+
+CalStruct cube(int32_t n, int32_t dim, int32_t dtype = BS_F64) {
+  CalStruct c;
+  for (int a = 0; a < 3; ++a) {
+    c.q[a].assign(n, 0);
+    c.d[a].assign(n, dim);
+  }
+  c.band = 0;
+  c.dtype = dtype;
+  if (dtype == BS_BF16_F32)
+    for (auto &f : c.flags) f |= BS_LAYOUT_ALIGN16;
+  return c;
+}
+
+// Charges -h..h with dims max(1, round(peak exp(-q^2 / width))), on all three axes.
+CalStruct gaussian(int32_t h, double peak, double width) {
+  CalStruct c;
+  for (int a = 0; a < 3; ++a)
+    for (int32_t q = -h; q <= h; ++q) {
+      c.q[a].push_back(q);
+      c.d[a].push_back(std::max(1, (int32_t)std::lround(peak * std::exp(-(double)q * q / width))));
+    }
+  return c;
+}
+
+struct CalRun {
+  double us = 0;            // median event-to-event time of bs_contract
+  double gather_ms = 0, zero_ms = 0;
+  double exec_tile = 0, exec_tail = 0, exec_general = 0;
+  bs_plan_stats st{};
+  int64_t stages_max = 0, tiles_max = 0;   // BF16: the busiest CTA's stages and tiles
+};
+
+// Build the structure's layouts and plan, run bs_contract `reps` times with
+// L2 emptied before each (a write over `flush`), and report medians.
+bs_status cal_run(const CalStruct &cs, bs_plan_options o, void *flush, size_t flush_bytes, cudaStream_t s,
+                  cudaEvent_t e0, cudaEvent_t e1, int reps, CalRun *out) {
+  bs_axis_desc ax[3];
+  for (int a = 0; a < 3; ++a) ax[a] = {(int32_t)cs.q[a].size(), cs.q[a].data(), nullptr, cs.d[a].data()};
+  const bs_rule rule{-cs.band, cs.band, 0};
+  const int32_t eb = cs.dtype == BS_F64 ? 8 : 2, ec = cs.dtype == BS_F64 ? 8 : 4;
+  bs_layout *A = nullptr, *B = nullptr;
+  bs_plan *P = nullptr;
+  void *da = nullptr, *db = nullptr, *dc = nullptr;
+  bs_status st = bs_layout_create(&ax[0], &ax[1], &rule, cs.flags[0], eb, &A);
+  if (st == BS_OK) st = bs_layout_create(&ax[1], &ax[2], &rule, cs.flags[1], eb, &B);
+  o.c_layout_flags = cs.flags[2];
+  o.host_only = 0;
+  o.profile = 1;
+  if (st == BS_OK) st = bs_plan_create(A, B, cs.dtype, &o, &P);
+  if (st == BS_OK) {
+    const size_t na = (size_t)std::max<int64_t>(A->nelems, 8) * eb, nb = (size_t)std::max<int64_t>(B->nelems, 8) * eb;
+    const size_t nc = (size_t)std::max<int64_t>(P->C.nelems, 8) * ec;
+    if (cudaMalloc(&da, na) != cudaSuccess || cudaMalloc(&db, nb) != cudaSuccess || cudaMalloc(&dc, nc) != cudaSuccess)
+      st = BS_ERR_OOM;
+    else if (cudaMemsetAsync(da, 0, na, s) != cudaSuccess || cudaMemsetAsync(db, 0, nb, s) != cudaSuccess)
+      st = BS_ERR_CUDA;
+  }
+  std::vector<double> t, g, z;
+  for (int r = 0; st == BS_OK && r < reps + 2; ++r) {
+    cudaMemsetAsync(flush, r, flush_bytes, s);
+    cudaEventRecord(e0, s);
+    st = bs_contract(P, da, db, dc, s);
+    cudaEventRecord(e1, s);
+    if (st != BS_OK) break;
+    if (cudaEventSynchronize(e1) != cudaSuccess) {
+      st = BS_ERR_CUDA;
+      break;
+    }
+    float ms = 0;
+    cudaEventElapsedTime(&ms, e0, e1);
+    bs_phase_times ph{};
+    bs_plan_profile(P, &ph);
+    if (r >= 2) {   // two warm-up runs
+      t.push_back(ms * 1e3);
+      g.push_back(ph.gather_ms);
+      z.push_back(ph.zero_ms);
+    }
+  }
+  if (st == BS_OK) st = bs_plan_last_device_error(P, s);
+  auto median = [](std::vector<double> v) {
+    if (v.empty()) return 0.0;
+    std::nth_element(v.begin(), v.begin() + v.size() / 2, v.end());
+    return v[v.size() / 2];
+  };
+  if (st == BS_OK) {
+    out->us = median(t);
+    out->gather_ms = median(g);
+    out->zero_ms = median(z);
+    out->exec_tile = P->ts.exec_tile;
+    out->exec_tail = P->ts.exec_tail;
+    out->exec_general = P->ts.exec_general;
+    out->st = P->stats;
+    for (const auto &c : P->bctas) {
+      out->stages_max = std::max<int64_t>(out->stages_max, c.stage_count);
+      out->tiles_max = std::max<int64_t>(out->tiles_max, c.task_count);
+    }
+  }
+  cudaFree(da);
+  cudaFree(db);
+  cudaFree(dc);
+  bs_plan_destroy(P);
+  bs_layout_destroy(A);
+  bs_layout_destroy(B);
+  return st;
+}
+
+// The cost-model constants of the planner, each from the run that isolates it.
+bs_status calibrate_model(bs_calibration *out, cudaStream_t s) {
+  const size_t flush_bytes = (size_t)256 << 20;
+  void *flush = nullptr;
+  cudaEvent_t e0, e1;
+  if (cudaMalloc(&flush, flush_bytes) != cudaSuccess) return BS_ERR_OOM;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  bs_plan_options o;
+  bs_plan_options_default(&o);
+  bs_status st = BS_OK;
+  do {
+    CalRun one, tile, tail, general, pack_small, pack_big, zero_big, bone, bdeep, bwide;
+    // a contraction with almost no work: launch, first-task chain, exit
+    if ((st = cal_run(cube(1, 1), o, flush, flush_bytes, s, e0, e1, 20, &one)) != BS_OK) break;
+    out->t_fixed_us = one.us;
+    // one dense 768^3 group: the tile path
+    if ((st = cal_run(cube(1, 768), o, flush, flush_bytes, s, e0, e1, 5, &tile)) != BS_OK) break;
+    out->tile_gflops = tile.exec_tile / std::max(1e-3, tile.us - one.us) / 1e3;
+    // the 31-charge tail (every group one view): the lane-packed tail path
+    CalStruct g31 = gaussian(15, 64.0, 50.0);
+    if ((st = cal_run(g31, o, flush, flush_bytes, s, e0, e1, 20, &tail)) != BS_OK) break;
+    out->tail_gflops = (tail.exec_tail + tail.exec_general) / std::max(1e-3, tail.us - one.us) / 1e3;
+    // the same with block-row operands, contraction axis, no gather: several views per group
+    CalStruct g31b = g31;
+    g31b.flags[0] = g31b.flags[1] = BS_LAYOUT_BLOCKROW;
+    bs_plan_options og = o;
+    og.axis_policy = BS_AXIS_CONTRACTION;
+    og.pack_policy = BS_PACK_NEVER;
+    if ((st = cal_run(g31b, og, flush, flush_bytes, s, e0, e1, 20, &general)) != BS_OK) break;
+    const double t_single = general.exec_tail / (out->tail_gflops * 1e3);
+    out->general_gflops = general.exec_general / std::max(1e-3, general.us - one.us - t_single) / 1e3;
+    // the gather, small (its fixed cost) and large (its bandwidth)
+    bs_plan_options op = og;
+    op.pack_policy = BS_PACK_ALWAYS;
+    if ((st = cal_run(g31b, op, flush, flush_bytes, s, e0, e1, 20, &pack_small)) != BS_OK) break;
+    out->pack_fixed_us = pack_small.gather_ms * 1e3;
+    CalStruct g41b = gaussian(20, 384.0, 60.0);
+    g41b.flags[0] = g41b.flags[1] = g41b.flags[2] = BS_LAYOUT_BLOCKROW;
+    if ((st = cal_run(g41b, op, flush, flush_bytes, s, e0, e1, 5, &pack_big)) != BS_OK) break;
+    out->pack_gbs = 2.0 * pack_big.st.packed_bytes / std::max(1e-3, pack_big.gather_ms * 1e3 - out->pack_fixed_us) / 1e3;
+    // the zero fill before atomic scatter, on the large structure's C
+    bs_plan_options oz = o;
+    oz.axis_policy = BS_AXIS_FREE;
+    oz.pack_policy = BS_PACK_NEVER;
+    if ((st = cal_run(gaussian(20, 384.0, 60.0), oz, flush, flush_bytes, s, e0, e1, 5, &zero_big)) != BS_OK) break;
+    // BF16: one 128 x 256 tile with one stage (fixed cost), one deep group
+    // (stages), many shallow groups (tiles)
+    CalStruct b1 = cube(1, 64, BS_BF16_F32);
+    b1.d[2].assign(1, 256);
+    b1.d[0].assign(1, 128);
+    if ((st = cal_run(b1, o, flush, flush_bytes, s, e0, e1, 20, &bone)) != BS_OK) break;
+    CalStruct b2 = cube(1, 256, BS_BF16_F32);
+    b2.d[0].assign(1, 128);
+    b2.d[1].assign(1, 8192);   // 128 stages of 64 on one CTA
+    if ((st = cal_run(b2, o, flush, flush_bytes, s, e0, e1, 10, &bdeep)) != BS_OK) break;
+    out->bf16_stage_us = std::max(0.0, bdeep.us - bone.us) / std::max<int64_t>(1, bdeep.stages_max - 1);
+    CalStruct b3 = cube(1, 64, BS_BF16_F32);
+    b3.d[0].assign(1, 128 * 152 * 8);   // eight 128 x 256 tiles of one stage on every CTA
+    b3.d[2].assign(1, 256);
+    if ((st = cal_run(b3, o, flush, flush_bytes, s, e0, e1, 10, &bwide)) != BS_OK) break;
+    out->bf16_tile_us = std::max(0.0, bwide.us - bone.us - (bwide.stages_max - 1) * out->bf16_stage_us) /
+                        std::max<int64_t>(1, bwide.tiles_max - 1);
+    // zero fill bandwidth: its populated C bytes over the measured phase
+    {
+      int64_t cbytes = 0;
+      CalStruct zs = gaussian(20, 384.0, 60.0);
+      // C of the free-axis plan: every populated block of the product, 8 bytes each
+      for (size_t i = 0; i < zs.q[0].size(); ++i)
+        for (size_t j = 0; j < zs.q[2].size(); ++j)
+          if (std::abs(zs.q[0][i] - zs.q[2][j]) <= 2) cbytes += (int64_t)zs.d[0][i] * zs.d[2][j] * 8;
+      out->zero_gbs = zero_big.zero_ms > 0 ? cbytes / (zero_big.zero_ms * 1e-3) / 1e9 : 0.0;
+    }
+  } while (false);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaFree(flush);
+  return st;
+}
+
 }  // namespace
 
 }  // namespace bs
@@ -58,6 +308,7 @@ __global__ void copy_probe(const double4_32a *src, double4_32a *dst, size_t n) {
 extern "C" bs_status bs_calibrate(bs_calibration *out, void *stream) {
   using namespace bs;
   if (!out) return BS_ERR_INVALID_ARG;
+  *out = bs_calibration{};
   cudaStream_t s = (cudaStream_t)stream;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BS_ERR_CUDA;
@@ -65,6 +316,7 @@ extern "C" bs_status bs_calibrate(bs_calibration *out, void *stream) {
   cudaEvent_t e0, e1;
   if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return BS_ERR_CUDA;
   double *scratch = nullptr;
+  ClockRec *recs = nullptr;
   void *bufs = nullptr;
   const size_t copy_bytes = (size_t)1 << 30;
   bs_status st = BS_OK;
@@ -79,17 +331,65 @@ extern "C" bs_status bs_calibrate(bs_calibration *out, void *stream) {
     return ms / reps;
   };
   do {
-    const int blocks = sms * 8, threads = 256;
-    if (cudaMalloc(&scratch, (size_t)blocks * threads * sizeof(double)) != cudaSuccess) {
+    // Probe shapes: CTAs per SM x threads x chains.  The best one is taken as the
+    // FP64 pipe's rate; its SM clock comes from the CTAs' cycle and time stamps.
+    const int max_blocks = sms * 8, threads = 256;
+    if (cudaMalloc(&scratch, (size_t)max_blocks * 1024 * sizeof(double)) != cudaSuccess ||
+        cudaMalloc(&recs, (size_t)max_blocks * sizeof(ClockRec)) != cudaSuccess) {
       st = BS_ERR_OOM;
       break;
     }
-    for (int variant = 0; variant < 2; ++variant) {
-      const int active = variant == 0 ? 32 : 8;
-      const double ms = timed([&] { dfma_probe<<<blocks, threads, 0, s>>>(scratch, 1.0, active); }, 5);
-      const double flops = 2.0 * 8 * kFmaIters * (double)blocks * (threads / 32) * active;
-      if (variant == 0) out->fp64_gflops = flops / (ms * 1e6);
-      else out->fp64_gflops_quarter_warp = flops / (ms * 1e6);
+    std::vector<ClockRec> host((size_t)max_blocks);
+    auto clock_mhz = [&](int blocks) {
+      cudaMemcpy(host.data(), recs, (size_t)blocks * sizeof(ClockRec), cudaMemcpyDeviceToHost);
+      std::vector<double> f;
+      for (int b = 0; b < blocks; ++b)
+        if (host[b].t1 > host[b].t0) f.push_back((double)(host[b].c1 - host[b].c0) / (double)(host[b].t1 - host[b].t0) * 1e3);
+      if (f.empty()) return 0.0;
+      std::nth_element(f.begin(), f.begin() + f.size() / 2, f.end());
+      return f[f.size() / 2];
+    };
+    struct Shape {
+      int per_sm, thr, chains;
+    };
+    const Shape shapes[] = {{8, 256, 8}, {4, 256, 8}, {2, 256, 8}, {4, 256, 16}, {1, 1024, 8}, {2, 512, 4}};
+    double best = 0.0, best_mhz = 0.0;
+    for (const Shape &sh : shapes) {
+      const int blocks = sms * sh.per_sm;
+      auto launch = [&] {
+        if (sh.chains == 4) dfma_probe<4><<<blocks, sh.thr, 0, s>>>(scratch, recs, 1.0, 32);
+        else if (sh.chains == 8) dfma_probe<8><<<blocks, sh.thr, 0, s>>>(scratch, recs, 1.0, 32);
+        else dfma_probe<16><<<blocks, sh.thr, 0, s>>>(scratch, recs, 1.0, 32);
+      };
+      const double ms = timed(launch, 3);
+      const double flops = 2.0 * sh.chains * kFmaIters * (double)blocks * sh.thr;
+      const double gf = flops / (ms * 1e6);
+      if (gf > best) {
+        best = gf;
+        best_mhz = clock_mhz(blocks);
+      }
+    }
+    out->fp64_gflops = best;
+    out->fp64_sm_mhz = best_mhz;
+    out->fp64_flop_per_clk_sm = best_mhz > 0 ? best * 1e3 / (sms * best_mhz) : 0.0;
+    {
+      const int blocks = sms * 8;
+      const double ms = timed([&] { dfma_probe<8><<<blocks, threads, 0, s>>>(scratch, nullptr, 1.0, 8); }, 3);
+      out->fp64_gflops_quarter_warp = 2.0 * 8 * kFmaIters * (double)blocks * (threads / 32) * 8 / (ms * 1e6);
+    }
+    {
+      double bestm = 0.0, mhz = 0.0;
+      for (int per_sm : {4, 8}) {
+        const int blocks = sms * per_sm;
+        const double ms = timed([&] { dmma_probe<<<blocks, threads, 0, s>>>(scratch, recs, 1.0); }, 3);
+        const double gf = 512.0 * 8 * (kFmaIters / 4) * (double)blocks * (threads / 32) / (ms * 1e6);
+        if (gf > bestm) {
+          bestm = gf;
+          mhz = clock_mhz(blocks);
+        }
+      }
+      out->fp64_dmma_gflops = bestm;
+      out->dmma_flop_per_clk_sm = mhz > 0 ? bestm * 1e3 / (sms * mhz) : 0.0;
     }
     out->launch_us = 1e3 * timed([&] { empty_kernel<<<1, 32, 0, s>>>(); }, 2000);
     if (cudaMalloc(&bufs, 2 * copy_bytes) != cudaSuccess) {
@@ -102,9 +402,21 @@ extern "C" bs_status bs_calibrate(bs_calibration *out, void *stream) {
     }, 10);
     out->copy_gbs = 2.0 * copy_bytes / (ms * 1e6);
     out->sm_count = sms;
+    st = calibrate_model(out, s);
+    if (st != BS_OK) break;
+    {
+      std::vector<int16_t> map;
+      if (sm_index_map(dev, sms, nullptr, s, &map) == BS_OK) {
+        int32_t bound = 0;
+        for (size_t t = 0; t < map.size(); ++t)
+          if (map[t] >= 0) bound = (int32_t)t + 1;
+        out->sm_id_bound = bound;
+      }
+    }
     if (cudaGetLastError() != cudaSuccess) st = BS_ERR_CUDA;
   } while (false);
   cudaFree(scratch);
+  cudaFree(recs);
   cudaFree(bufs);
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);

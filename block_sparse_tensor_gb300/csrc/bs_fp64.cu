@@ -57,7 +57,6 @@ struct TileSmem {
   int64_t kL[kKC];
   int64_t kB[kKC];
   int task;
-  int q0, qk;   // tail: this SM's queue and how many queues were emptied
 };
 
 __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
@@ -133,8 +132,8 @@ __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
 __device__ void run_tail_warp(const Fp64Params &p, int w) {
   const int lane = threadIdx.x & 31;
   const int e = w * 32 + lane;
-  const bool ok = e < p.ntail;
-  const int2 el = ok ? p.tail_elems[e] : make_int2(p.tail_elems[w * 32].x, 0);
+  const int2 el = e < p.ntail ? p.tail_elems[e] : make_int2(p.tail_elems[w * 32].x, kTailPad);
+  const bool ok = el.y != kTailPad;   // a padding entry holds no output
   const int r = el.y >> 16, c = el.y & 0xFFFF;
   // single-segment groups: addressing resolved at plan time, one table load
   const TailDesc D = p.tdesc[el.x];
@@ -214,6 +213,16 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
   }
 }
 
+// The tail queue of the SM this CTA runs on: the SM's dense index (the
+// hardware identifiers may skip values), modulo the queue count.
+__device__ __forceinline__ int home_queue(const Fp64Params &p) {
+  unsigned smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  int idx = (int)smid;
+  if ((int)smid < p.nsm_ids && p.sm_queue[smid] >= 0) idx = p.sm_queue[smid];
+  return idx % p.nq;
+}
+
 // Two instances: four CTAs per SM (64 registers a thread) for plans with tile
 // tasks, whose shared-memory staging wants the most resident warps, and three
 // for plans made only of tail tasks, which measure faster with fewer, quicker
@@ -230,37 +239,49 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Pa
     if (t >= p.ntasks) break;
     run_tile(p, p.tasks[t], sm);
   }
-  // then the tail tasks: first the queue dealt to this SM, then, once it is
-  // empty, whatever is left in the others (so no output depends on every SM
-  // receiving CTAs).  Thread 0 finds the next task; the CTA runs it, warp w on
-  // the task's w-th 32 outputs.
+  // Then the tail: CTA-sized tasks (kThreads consecutive outputs of the tail
+  // list, so the 8 warps walk the same B rows through L1), dealt at plan time
+  // longest first onto one queue per SM, each queue's tasks numbered
+  // consecutively.  A CTA serves the queue of the SM it runs on, claiming the
+  // queue's next task while it still runs the current one; once that queue is
+  // empty it takes tasks from the others (so no output depends on every SM
+  // receiving CTAs).  Thread 0 claims; the CTA runs the task, warp w on its
+  // w-th 32 outputs.
   if (p.nct > 0) {
-    if (threadIdx.x == 0) {
-      unsigned smid;
-      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-      sm.q0 = (int)(smid % (unsigned)p.nq);
-      sm.qk = 0;
-    }
     const int warp = threadIdx.x >> 5;
+    int q0 = 0, qk = 0;          // thread 0: home queue, queues emptied so far
+    unsigned nx = 0;             // thread 0: claim on the home queue made during the last task
+    bool have_nx = false;
+    if (threadIdx.x == 0) q0 = home_queue(p);
     for (;;) {
       if (threadIdx.x == 0) {
         int got = -1;
-        while (sm.qk < p.nq) {
-          if (sm.qk > 0 && *(volatile uint32_t *)&p.counter[2] >= (uint32_t)p.nct) {   // all taken
-            sm.qk = p.nq;
-            break;
+        while (qk < p.nq) {
+          const int q = q0 + qk < p.nq ? q0 + qk : q0 + qk - p.nq;
+          const int beg = p.qptr[q], n = p.qptr[q + 1] - beg;
+          unsigned i;
+          if (qk == 0 && have_nx) {
+            i = nx;
+            have_nx = false;
+          } else {
+            if (qk > 0 && *(volatile uint32_t *)&p.counter[2] >= (uint32_t)p.nct) {   // all taken
+              qk = p.nq;
+              break;
+            }
+            i = atomicAdd(&p.counter[kQueueCounterBase + q], 1u);
           }
-          const int q = sm.q0 + sm.qk < p.nq ? sm.q0 + sm.qk : sm.q0 + sm.qk - p.nq;
-          const int beg = p.tq_ptr[q], n = p.tq_ptr[q + 1] - beg;
-          const int i = (int)atomicAdd(&p.counter[kQueueCounterBase + q], 1u);
-          if (i < n) {
+          if (i < (unsigned)n) {
             atomicAdd(&p.counter[2], 1u);
-            got = p.tq_items[beg + i];
+            got = beg + (int)i;
             break;
           }
-          ++sm.qk;
+          ++qk;
         }
         sm.task = got;
+        if (got >= 0 && qk == 0) {   // the next claim travels while this task runs
+          nx = atomicAdd(&p.counter[kQueueCounterBase + q0], 1u);
+          have_nx = true;
+        }
       }
       __syncthreads();
       const int ct = sm.task;
@@ -271,32 +292,103 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Pa
     }
   }
   __syncthreads();
-  // The last CTA to leave returns the counters to zero for the next launch.
-  // Every CTA has taken its final work index before it counts itself out.
+  // The last CTA to leave returns the counters to zero for the next launch,
+  // all of its threads at once.  Every CTA has taken its final work index
+  // before it counts itself out.
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned prev = atomicAdd(&p.counter[1], 1u);
-    if (prev == gridDim.x - 1) {
+    sm.task = atomicAdd(&p.counter[1], 1u) == gridDim.x - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (sm.task) {
+    for (int q = threadIdx.x; q < p.nq; q += kThreads) atomicExch(&p.counter[kQueueCounterBase + q], 0u);
+    if (threadIdx.x == 0) {
       atomicExch(&p.counter[0], 0u);
       atomicExch(&p.counter[2], 0u);
-      for (int q = 0; q < p.nq; ++q) atomicExch(&p.counter[kQueueCounterBase + q], 0u);
-      atomicExch(&p.counter[1], 0u);
     }
+    __syncthreads();
+    if (threadIdx.x == 0) atomicExch(&p.counter[1], 0u);
   }
+}
+
+// The gather: one warp per block copy, copies listed largest first at plan
+// time and dealt to the warps in turn (each warp fetches its next copy's
+// descriptor while it moves the current one).  No element index is divided:
+//   - a copy whose rows are contiguous in both buffers (ld = cols on both
+//     sides) is one flat range, moved 16 bytes per lane when both ends are
+//     16-byte aligned;
+//   - rows of at most 32 elements: each lane keeps one (row offset, column)
+//     pair for the whole copy, so a warp moves floor(32 / cols) rows a step;
+//   - wider rows: the lanes walk each row, 16 bytes at a time when every row
+//     of both views starts on a 16-byte boundary.
+template <class T, int kUnroll>
+__device__ __forceinline__ void copy_span(const T *__restrict__ s, T *__restrict__ d, int n, int lane, bool vec) {
+  constexpr int V = 16 / (int)sizeof(T);
+  int x0 = 0;
+  if (vec) {
+    const int nv = n / V;   // whole 16-byte units
+    const int4 *sv = (const int4 *)s;
+    int4 *dv = (int4 *)d;
+    int u = lane;
+    for (; u + 32 * (kUnroll - 1) < nv; u += 32 * kUnroll) {
+      int4 t[kUnroll];
+#pragma unroll
+      for (int q = 0; q < kUnroll; ++q) t[q] = __ldg(sv + u + 32 * q);
+#pragma unroll
+      for (int q = 0; q < kUnroll; ++q) dv[u + 32 * q] = t[q];
+    }
+    for (; u < nv; u += 32) dv[u] = __ldg(sv + u);
+    x0 = nv * V;
+  }
+  int x = x0 + lane;
+  for (; x + 32 * (kUnroll - 1) < n; x += 32 * kUnroll) {
+    T t[kUnroll];
+#pragma unroll
+    for (int q = 0; q < kUnroll; ++q) t[q] = __ldg(s + x + 32 * q);
+#pragma unroll
+    for (int q = 0; q < kUnroll; ++q) d[x + 32 * q] = t[q];
+  }
+  for (; x < n; x += 32) d[x] = __ldg(s + x);
 }
 
 template <class T>
 __global__ void pack_kernel(PackParams a, PackParams b, int32_t ntotal) {
-  for (int c = blockIdx.x; c < ntotal; c += gridDim.x) {
-    const bool is_a = c < a.ncopies;
-    const PackParams &pp = is_a ? a : b;
-    const PackCopy cp = pp.copies[c];
-    const T *src = (const T *)pp.src + cp.src;
-    T *dst = (T *)pp.dst + cp.dst;
-    const int n = cp.rows * cp.cols;
-    for (int e = threadIdx.x; e < n; e += blockDim.x) {
-      const int r = e / cp.cols, q = e - r * cp.cols;
-      dst[(int64_t)r * cp.dst_ld + q] = src[(int64_t)r * cp.src_ld + q];
+  constexpr int V = 16 / (int)sizeof(T);
+  const int lane = threadIdx.x & 31;
+  const int nw = (int)(gridDim.x * (blockDim.x >> 5));
+  int c = (int)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
+  PackCopy cp;
+  if (c < ntotal) cp = a.copies[c];
+  for (; c < ntotal; c += nw) {
+    const PackCopy cur = cp;
+    if (c + nw < ntotal) cp = a.copies[c + nw];   // the next descriptor, in flight meanwhile
+    const PackParams &pp = c < a.ncopies ? a : b;
+    const T *src = (const T *)pp.src + cur.src;
+    T *dst = (T *)pp.dst + cur.dst;
+    const bool base16 = (((uintptr_t)pp.src | (uintptr_t)pp.dst) & 15u) == 0;
+    if (cur.src_ld == cur.cols && cur.dst_ld == cur.cols) {
+      const bool vec = base16 && ((cur.src | cur.dst) % V) == 0;
+      copy_span<T, 4>(src, dst, cur.rows * cur.cols, lane, vec);
+    } else if (cur.cols <= 32) {
+      const int rpw = 32 / cur.cols;
+      const int lr = lane / cur.cols, lc = lane - lr * cur.cols;
+      if (lr < rpw) {
+        const T *sp = src + lc;
+        T *dp = dst + lc;
+        int r = lr;
+        for (; r + 3 * rpw < cur.rows; r += 4 * rpw) {
+          T t[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) t[q] = __ldg(sp + (int64_t)(r + q * rpw) * cur.src_ld);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dp[(int64_t)(r + q * rpw) * cur.dst_ld] = t[q];
+        }
+        for (; r < cur.rows; r += rpw) dp[(int64_t)r * cur.dst_ld] = __ldg(sp + (int64_t)r * cur.src_ld);
+      }
+    } else {
+      const bool vec = base16 && ((cur.src | cur.dst | cur.src_ld | cur.dst_ld) % V) == 0;
+      for (int r = 0; r < cur.rows; ++r)
+        copy_span<T, 2>(src + (int64_t)r * cur.src_ld, dst + (int64_t)r * cur.dst_ld, cur.cols, lane, vec);
     }
   }
 }
@@ -355,7 +447,8 @@ int fp64_max_ctas_per_sm(bool tail_only) {
 
 cudaError_t launch_pack2(const PackParams &a, const PackParams &b, int32_t ntotal, int grid, cudaStream_t s) {
   if (ntotal <= 0) return cudaSuccess;
-  grid = grid < ntotal ? grid : ntotal;
+  const int need = (ntotal + 7) / 8;   // one warp per copy, eight warps a CTA
+  grid = grid < need ? grid : need;
   if (a.elem_bytes == 8) pack_kernel<double><<<grid, 256, 0, s>>>(a, b, ntotal);
   else pack_kernel<uint16_t><<<grid, 256, 0, s>>>(a, b, ntotal);
   return cudaGetLastError();

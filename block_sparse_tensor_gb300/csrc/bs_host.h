@@ -63,6 +63,18 @@ cudaError_t launch_control_fp64(const double *A, const double *B, double *C, int
 cudaError_t launch_control_bf16(const uint16_t *A, const uint16_t *B, float *C, int64_t a_off, int64_t lda,
                                 int64_t b_off, int64_t ldb, int64_t c_off, int64_t ldc, int m, int n, int k,
                                 cudaStream_t s);
+// Dense SM index per hardware SM identifier (-1: not seen), found once per
+// device by a short probe launch on `s` (into dev_buf, or a temporary
+// allocation when it is NULL; dev_buf needs sm_probe_bytes(sm_count) bytes).
+size_t sm_probe_bytes(int sm_count);
+bs_status sm_index_map(int device, int sm_count, void *dev_buf, cudaStream_t s, std::vector<int16_t> *out);
+// Queue bounds and SM map of the FP64 tail, copied into the kernel parameters.
+inline void fill_queue_params(Fp64Params *p, const std::vector<int32_t> &tq_ptr, const std::vector<int16_t> &sm_map) {
+  p->nq = tq_ptr.size() > 1 ? (int32_t)tq_ptr.size() - 1 : 0;
+  for (int q = 0; q <= kMaxQueues; ++q) p->qptr[q] = q < (int)tq_ptr.size() ? tq_ptr[q] : 0;
+  p->nsm_ids = sm_map.size() <= (size_t)kMaxSmIds ? (int32_t)sm_map.size() : 0;
+  for (int i = 0; i < kMaxSmIds; ++i) p->sm_queue[i] = i < p->nsm_ids ? sm_map[i] : (int16_t)-1;
+}
 // Resident CTAs per SM of the FP64 kernel instance a plan with (false) or
 // without (true) tile tasks launches.
 int fp64_max_ctas_per_sm(bool tail_only);

@@ -123,6 +123,11 @@ constexpr int kQueueCounterBase = 64;   // in uint32 units
 // Device status word values (first int of the status buffer).
 enum DeviceStatus : int32_t { DS_OK = 0, DS_TIMEOUT = 1, DS_BOUNDS = 2 };
 
+constexpr int kMaxQueues = 160;   // tail queues: one per SM, at most this many
+constexpr int kMaxSmIds = 256;    // hardware SM identifiers the parameter map covers
+// Tail-list entry that pads a tail task to kThreads outputs: no output.
+constexpr int32_t kTailPad = 0x7FFF7FFF;
+
 struct Fp64Params {
   const double *A;
   const double *B;
@@ -131,17 +136,19 @@ struct Fp64Params {
   const Group *groups;
   const RowSeg *rsegs;
   const KSeg *ksegs;
-  const int2 *tail_elems;
+  const int2 *tail_elems;  // tail task t covers tail_elems[kThreads t .. kThreads t + kThreads - 1]
   const TailDesc *tdesc;   // per group (used for tail groups)
-  const int32_t *tq_ptr;    // per-SM queues of tail tasks: queue q holds tq_items[tq_ptr[q] .. tq_ptr[q+1])
-  const int32_t *tq_items;  // tail task t covers tail_elems[kThreads t .. kThreads t + kThreads - 1]
   int32_t ntasks;
-  int32_t ntail;       // outputs in the tail list
+  int32_t ntail;       // entries of the tail list (a multiple of kThreads, padding included)
   int32_t nct;         // tail tasks
   int32_t nq;          // queues (one per SM of the planned device)
   uint32_t *counter;   // [0] next tile task, [1] CTAs finished, [2] tail tasks taken;
-                       // counter[64 + q]: next item of queue q.  All return to 0 at exit.
+                       // counter[64 + q]: next task of queue q.  All return to 0 at exit.
   int32_t *status;
+  int32_t nsm_ids;     // entries of sm_queue in use (0: take %smid modulo nq)
+  // Kept in the parameters, so a CTA finds its first task without a memory load:
+  int32_t qptr[kMaxQueues + 1];   // queue q holds tail tasks qptr[q] .. qptr[q+1]-1 (consecutive)
+  int16_t sm_queue[kMaxSmIds];    // dense SM index per hardware SM identifier, -1 if unknown
 };
 
 struct PackParams {

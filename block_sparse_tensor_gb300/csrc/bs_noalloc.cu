@@ -19,6 +19,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "bs_plan.h"
 
@@ -72,8 +73,6 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   const size_t n_ksegs = P->gs.ksegs.size() * sizeof(KSeg);
   const size_t n_tail = P->ts.tail_elems.size() * sizeof(int32_t);
   const size_t n_tdesc = P->ts.tdesc.size() * sizeof(TailDesc);
-  const size_t n_tqp = P->ts.tq_ptr.size() * sizeof(int32_t);
-  const size_t n_tqi = P->ts.tq_items.size() * sizeof(int32_t);
   const int nq = (int)std::max<size_t>(1, P->ts.tq_ptr.size()) - 1;
   const size_t n_ctr = counter_bytes(nq);
   const size_t n_pack = P->pack_copies.size() * sizeof(PackCopy);
@@ -93,10 +92,6 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   off = align256(off + n_tail);
   const size_t o_tdesc = off;
   off = align256(off + n_tdesc);
-  const size_t o_tqp = off;
-  off = align256(off + n_tqp);
-  const size_t o_tqi = off;
-  off = align256(off + n_tqi);
   const size_t o_pack = off;
   off = align256(off + n_pack);
   const size_t o_zero = off;
@@ -114,7 +109,16 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BS_ERR_CUDA;
-  per_sm = std::max(1, fp64_max_ctas_per_sm(P->ts.tasks.empty()));
+  // the grid bs_contract launches for this plan: the plan's CTAs per SM, else the occupancy limit
+  per_sm = P->opts.ctas_per_sm > 0 ? P->opts.ctas_per_sm : std::max(1, fp64_max_ctas_per_sm(P->ts.tasks.empty()));
+
+  // the SM numbering of this device, found once (its probe writes into the array's head)
+  std::vector<int16_t> sm_map;
+  if (P->ts.tq_ptr.size() > 1) {
+    if (sm_probe_bytes(sms) > kNoAllocScratchBytes) return BS_ERR_OVERFLOW;
+    st = sm_index_map(dev, sms, b, s, &sm_map);
+    if (st != BS_OK) return st;
+  }
 
   auto up = [&](size_t o, const void *src, size_t n) -> bool {
     return n == 0 || cudaMemcpyAsync(b + o, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
@@ -124,8 +128,7 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   if (!up(o_tasks, P->ts.tasks.data(), n_tasks) || !up(o_groups, P->gs.groups.data(), n_groups) ||
       !up(o_rsegs, P->gs.rsegs.data(), n_rsegs) || !up(o_ksegs, P->gs.ksegs.data(), n_ksegs) ||
       !up(o_tail, P->ts.tail_elems.data(), n_tail) || !up(o_tdesc, P->ts.tdesc.data(), n_tdesc) ||
-      !up(o_tqp, P->ts.tq_ptr.data(), n_tqp) ||
-      !up(o_tqi, P->ts.tq_items.data(), n_tqi) || !up(o_pack, P->pack_copies.data(), n_pack) ||
+      !up(o_pack, P->pack_copies.data(), n_pack) ||
       !up(o_zero, P->zero_blocks.data(), n_zero))
     return BS_ERR_CUDA;
 
@@ -161,9 +164,7 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   p.ntasks = (int32_t)P->ts.tasks.size();
   p.ntail = (int32_t)ntail;
   p.nct = (int32_t)((ntail + kThreads - 1) / kThreads);
-  p.nq = nq;
-  p.tq_ptr = (const int32_t *)(b + o_tqp);
-  p.tq_items = (const int32_t *)(b + o_tqi);
+  fill_queue_params(&p, P->ts.tq_ptr, sm_map);
   p.counter = (uint32_t *)b;
   p.status = (int32_t *)(b + 128);
   const int64_t items = (int64_t)P->ts.tasks.size() + (ntail + kThreads - 1) / kThreads;

@@ -48,7 +48,7 @@ struct Entry {
 // One group per C block: the inner blocks in A's storage order, merged into
 // runs where both the A view and the B view continue with the same stride.
 GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C, bool merge_rows,
-                                 bool atomic, bool unchecked) {
+                                 bool atomic, bool unchecked, const std::vector<uint8_t> *cmask) {
   Builder bd;
   GroupSet &gs = bd.gs;
   gs.tptr.push_back(0);
@@ -74,6 +74,10 @@ GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const b
     for (int32_t j : touched) {
       auto &ent = bucket[j];
       const int32_t cb = C.find(i, j);
+      if (cmask && !(*cmask)[cb]) {   // another shard's C block
+        ent.clear();
+        continue;
+      }
       const bs_block_info &cbi = C.blocks[cb];
       bool merged = false;
       if (merge_rows && last_group[j] >= 0 && last_row[j] == i - 1 && last_entries[j].size() == ent.size()) {
@@ -161,7 +165,8 @@ GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const b
 // One group per (k, j): the A blocks of inner sector k stacked in A's storage
 // order; runs whose A rows and C rows continue with one stride share a row
 // segment.  Several groups add into the same C block, so stores are atomic.
-GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C) {
+GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C,
+                          const std::vector<uint8_t> *cmask) {
   Builder bd;
   GroupSet &gs = bd.gs;
   gs.tptr.push_back(0);
@@ -199,7 +204,9 @@ GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layou
       for (int64_t t = A.col_ptr[k]; t < A.col_ptr[k + 1]; ++t) {
         const auto &a = A.blocks[A.col_blk[t]];
         const int32_t i = a.row;
-        const auto &c = C.blocks[cblk[(t - A.col_ptr[k]) * nb + (u - B.row_ptr[k])]];
+        const int32_t cb = cblk[(t - A.col_ptr[k]) * nb + (u - B.row_ptr[k])];
+        if (cmask && !(*cmask)[cb]) continue;   // another shard's C block
+        const auto &c = C.blocks[cb];
         bool join = false;
         if ((int32_t)gs.rsegs.size() > g.rseg_begin) {
           RowSeg &s = gs.rsegs.back();
@@ -221,6 +228,7 @@ GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layou
         r += a.rows;
         bd.add_triple(i, k, j);
       }
+      if (r == 0) continue;   // every row of this (k, j) belongs to other shards
       g.m = r;
       g.rseg_count = (int32_t)gs.rsegs.size() - g.rseg_begin;
       g.kseg_begin = (int32_t)gs.ksegs.size();
@@ -241,7 +249,8 @@ GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layou
 }
 
 // No coalescing: one group per populated triple, scattered atomically.
-GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C) {
+GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C,
+                            const std::vector<uint8_t> *cmask) {
   Builder bd;
   GroupSet &gs = bd.gs;
   gs.tptr.push_back(0);
@@ -251,7 +260,9 @@ GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_lay
       const int32_t k = a.col;
       for (int64_t u = B.row_ptr[k]; u < B.row_ptr[k + 1]; ++u) {
         const auto &b = B.blocks[B.row_blk[u]];
-        const auto &c = C.blocks[C.find(i, b.col)];
+        const int32_t cb = C.find(i, b.col);
+        if (cmask && !(*cmask)[cb]) continue;   // another shard's C block
+        const auto &c = C.blocks[cb];
         Group g{};
         g.m = a.rows;
         g.n = b.cols;
@@ -280,6 +291,33 @@ GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_lay
       }
     }
   return gs;
+}
+
+std::vector<uint8_t> shard_mask(const bs_layout &A, const bs_layout &B, const bs_layout &C, int rank, int world) {
+  const size_t nc = C.blocks.size();
+  std::vector<double> cost(nc, 0.0);
+  for (int32_t i = 0; i < A.rows.n; ++i)
+    for (int64_t t = A.row_ptr[i]; t < A.row_ptr[i + 1]; ++t) {
+      const int32_t k = A.blocks[A.row_blk[t]].col;
+      const double dik = (double)A.rows.d[i] * A.cols.d[k];
+      for (int64_t u = B.row_ptr[k]; u < B.row_ptr[k + 1]; ++u) {
+        const int32_t j = B.blocks[B.row_blk[u]].col;
+        cost[C.find(i, j)] += dik * B.cols.d[j];
+      }
+    }
+  std::vector<int32_t> order(nc);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+  std::vector<double> load((size_t)world, 0.0);
+  std::vector<uint8_t> mask(nc, 0);
+  for (int32_t b : order) {
+    int best = 0;
+    for (int r = 1; r < world; ++r)
+      if (load[r] < load[best]) best = r;
+    load[best] += cost[b];
+    if (best == rank) mask[b] = 1;
+  }
+  return mask;
 }
 
 // Triples of every group, group by group, with merged rows folded in.
@@ -327,8 +365,8 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
   ts->tasks.clear();
   ts->tail_elems.clear();
   ts->tq_ptr.clear();
-  ts->tq_items.clear();
   ts->tdesc.clear();
+  ts->exec_tile = ts->exec_tail = ts->exec_general = ts->max_tail_task = 0;
   if (materialize) ts->tdesc.assign(gs.groups.size(), TailDesc{});
   std::vector<std::pair<double, Task>> costed;
   std::vector<int32_t> tails;
@@ -356,6 +394,7 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
         t.tn = std::min(tn, G.n - n0);
         const double slots = (double)lanes((int64_t)t.tm * t.tn);
         exec += 2.0 * slots * G.k;
+        ts->exec_tile += 2.0 * slots * G.k;
         costed.push_back({slots * G.k + pm.task_slots, t});
       }
   }
@@ -384,19 +423,43 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
     if (!pm.bucket_pad) return ka > kb;   // exact: by K only, as listed
     return std::make_tuple(-ka, ma, na) < std::make_tuple(-kb, mb, nb);
   });
-  if (!materialize) {
-    // The executed flops of the tail list without listing it: each warp of
-    // 32 consecutive outputs runs its first output's K, and the outputs of
-    // the sorted groups follow one another.
+  // The executed flops of the tail list without listing it: each warp of 32
+  // consecutive outputs runs its first output's K, and the outputs of the
+  // sorted groups follow one another.  Split by path: groups of one view
+  // (row and inner) take the unrolled loop, the others the segment walk.
+  {
     int64_t off = 0;
     for (int32_t g : tails) {
       int32_t mp, np, kp;
       padded(g, &mp, &np, &kp);
       const int64_t end = off + (int64_t)mp * np;
       const int64_t warps = (end + 31) / 32 - (off + 31) / 32;   // warp starts inside [off, end)
-      exec += 2.0 * 32.0 * kp * (double)warps;
+      const double ex = 2.0 * 32.0 * kp * (double)warps;
+      const Group &G = gs.groups[g];
+      if (G.rseg_count == 1 && G.kseg_count == 1) ts->exec_tail += ex;
+      else ts->exec_general += ex;
       off = end;
     }
+  }
+  // The costliest tail task is the first one (the list runs longest K first):
+  // each of its warps runs its first output's K.
+  {
+    int64_t off = 0;
+    int wstart = 0;
+    for (int32_t g : tails) {
+      int32_t mp, np, kp;
+      padded(g, &mp, &np, &kp);
+      const int64_t end = off + (int64_t)mp * np;
+      while (wstart < kThreads && wstart < end) {
+        ts->max_tail_task += 2.0 * 32.0 * kp;
+        wstart += 32;
+      }
+      off = end;
+      if (wstart >= kThreads) break;
+    }
+  }
+  if (!materialize) {
+    exec += ts->exec_tail + ts->exec_general;
     for (auto &c : costed) ts->tasks.push_back(c.second);
     ts->executed_flops = exec;
     return;
@@ -437,7 +500,7 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
   // arrive in.  Lane 0 of each warp holds that warp's longest K.
   const int nct = (int)((elem_k.size() + kThreads - 1) / kThreads);
   // no more queues than a few tasks each can fill (SMs then share a queue)
-  const int nq = std::max(1, std::min(pm.sms, nct / 4));
+  const int nq = std::max(1, std::min(std::min(pm.sms, kMaxQueues), nct / 4));
   std::vector<std::vector<int32_t>> queues(nq);
   std::vector<std::pair<double, int>> heap;   // (load, queue) min-heap
   for (int q = 0; q < nq; ++q) heap.push_back({0.0, q});
@@ -454,11 +517,28 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
     queues[heap.back().second].push_back(ct);
     std::push_heap(heap.begin(), heap.end(), cmp);
   }
+  // Renumber the tasks queue after queue, so queue q holds tasks
+  // tq_ptr[q] .. tq_ptr[q+1]-1 and a claim needs no table: the tail list is
+  // rewritten in that order, each task's kThreads entries together, the last
+  // (partial) task padded with entries that hold no output.
   ts->tq_ptr.assign(nq + 1, 0);
-  ts->tq_items.clear();
+  std::vector<int32_t> listed;
+  listed.swap(ts->tail_elems);
+  ts->tail_elems.reserve((size_t)nct * kThreads * 2);
+  const size_t nel = listed.size() / 2;
   for (int q = 0; q < nq; ++q) {
-    ts->tq_items.insert(ts->tq_items.end(), queues[q].begin(), queues[q].end());
-    ts->tq_ptr[q + 1] = (int32_t)ts->tq_items.size();
+    for (int32_t ct : queues[q]) {
+      for (size_t e = (size_t)ct * kThreads; e < (size_t)(ct + 1) * kThreads; ++e) {
+        if (e < nel) {
+          ts->tail_elems.push_back(listed[2 * e]);
+          ts->tail_elems.push_back(listed[2 * e + 1]);
+        } else {
+          ts->tail_elems.push_back(listed[2 * (nel - 1)]);   // a real group, so its descriptor can be read
+          ts->tail_elems.push_back(kTailPad);
+        }
+      }
+    }
+    ts->tq_ptr[q + 1] = ts->tq_ptr[q] + (int32_t)queues[q].size();
   }
   // longest processing time first for the dynamic scheduler
   std::stable_sort(costed.begin(), costed.end(),
@@ -467,8 +547,15 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
   ts->executed_flops = exec;
 }
 
-double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm, int64_t pack_bytes, int launches) {
-  const double compute = ts.executed_flops / (pm.fp64_gflops * 1e3);
+double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm, int64_t pack_bytes, int launches,
+                     int64_t zero_bytes) {
+  // Flop time of each path at its measured rate; the tail also cannot end
+  // before its costliest task has run at its share of one SM (the SM's CTAs
+  // split its FP64 pipe evenly).
+  const double sm_share_gflops = pm.tail_gflops / std::max(1, pm.parallel_ctas);
+  const double tail = std::max(ts.exec_tail / (pm.tail_gflops * 1e3) + ts.exec_general / (pm.general_gflops * 1e3),
+                               ts.max_tail_task / (sm_share_gflops * 1e3));
+  const double compute = ts.exec_tile / (pm.fp64_gflops * 1e3) + tail;
   int64_t nseg = 0, natomic_elems = 0;
   for (const auto &g : gs.groups) {
     nseg += g.kseg_count + g.rseg_count;
@@ -476,9 +563,24 @@ double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm,
   }
   const double par = std::max(1, pm.parallel_ctas);
   const double overhead = ((double)ts.tasks.size() * pm.t_task_us + (double)nseg * pm.t_segment_us) / par;
-  const double atomics = pm.atomic_penalty * natomic_elems * 8.0 / (pm.pack_gbs * 1e3);
-  const double pack = pack_bytes > 0 ? 2.0 * pack_bytes / (pm.pack_gbs * 1e3) : 0.0;
-  return compute + overhead + atomics + pack + launches * pm.t_launch_us;
+  const double atomics = pm.atomic_penalty * natomic_elems * 8.0 / (pm.zero_gbs * 1e3);
+  const double zero = zero_bytes > 0 ? (double)zero_bytes / (pm.zero_gbs * 1e3) : 0.0;
+  const double pack = pack_bytes > 0 ? pm.pack_fixed_us + 2.0 * pack_bytes / (pm.pack_gbs * 1e3) : 0.0;
+  return pm.t_fixed_us + std::max(0, launches - 1) * pm.t_launch_us + compute + overhead + atomics + zero + pack;
+}
+
+double model_bf16_us(const bs_plan &P, const PlanModel &pm) {
+  // One CTA per SM walks its own list: per CTA, its K stages and its output
+  // tiles (epilogue in proportion to the tile width); the slowest CTA ends it.
+  double worst = 0;
+  for (const auto &c : P.bctas) {
+    double t = c.stage_count * pm.bf16_stage_us;
+    for (int32_t i = 0; i < c.task_count; ++i) t += pm.bf16_tile_us * P.bstasks[c.task_begin + i].bn / 256.0;
+    worst = std::max(worst, t);
+  }
+  const double pack = P.stats.packed_bytes > 0 ? pm.pack_fixed_us + 2.0 * P.stats.packed_bytes / (pm.pack_gbs * 1e3)
+                                               : 0.0;
+  return pm.t_fixed_us + worst + pack;
 }
 
 }  // namespace bs

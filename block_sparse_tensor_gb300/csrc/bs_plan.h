@@ -5,6 +5,8 @@
 
 #include "bs_host.h"
 
+struct bs_plan;
+
 namespace bs {
 
 struct GroupSet {
@@ -22,35 +24,62 @@ struct TileSet {
   std::vector<Task> tasks;
   std::vector<int32_t> tail_elems;   // pairs: group, r << 16 | c
   std::vector<TailDesc> tdesc;       // per group: resolved addressing of single-segment tail groups
-  std::vector<int32_t> tq_ptr;       // per-SM queues of tail warp-tasks (LPT-balanced)
-  std::vector<int32_t> tq_items;
+  std::vector<int32_t> tq_ptr;       // per-SM queues of tail tasks (LPT-balanced): queue q holds
+                                     // tasks tq_ptr[q] .. tq_ptr[q+1]-1 of the tail list
   double executed_flops = 0;
+  // the same split by path: tile tasks, tail groups of one view (the unrolled
+  // loop), tail groups of several views (the segment walk)
+  double exec_tile = 0, exec_tail = 0, exec_general = 0;
+  double max_tail_task = 0;   // executed flops of the costliest tail task
 };
 
+// Cost model of one contraction (microseconds).  The defaults are this
+// build's measurements on a GB300; bs_calibrate measures them on the running
+// device and bs_calibration_apply hands them to the planner.
 struct PlanModel {
-  double t_launch_us = 2.0;
+  double t_launch_us = 2.0;      // each kernel of a contraction after the first
   double t_task_us = 0.4;
   double t_segment_us = 0.03;
-  double pack_gbs = 3000.0;
-  double fp64_gflops = 1200.0;
+  double pack_gbs = 3700.0;
+  double pack_fixed_us = 8.0;
+  double fp64_gflops = 1150.0;   // tile path, useful = executed
+  double tail_gflops = 900.0;    // tail path, one view per group, executed flops
+  double general_gflops = 300.0; // tail path, several views per group
+  double zero_gbs = 3000.0;
+  double t_fixed_us = 10.0;      // a contraction whose kernel has almost no work
   double atomic_penalty = 0.5;
+  double bf16_stage_us = 0.5;
+  double bf16_tile_us = 2.8;
   double task_slots = 4096;   // LPT weight of a task's fixed cost, in lane-flop units
   int parallel_ctas = 456;
   int sms = 152;
   bool bucket_pad = false;    // pad single-segment tail groups to power-of-two shapes
 };
 
+// `cmask` (indexed by C block, may be null): only the triples whose C block it
+// marks are grouped (a shard of the contraction); null groups every triple.
 GroupSet make_contraction_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C, bool merge_rows,
-                                 bool atomic, bool unchecked = false);
-GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C);
-GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C);
+                                 bool atomic, bool unchecked = false, const std::vector<uint8_t> *cmask = nullptr);
+GroupSet make_free_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C,
+                          const std::vector<uint8_t> *cmask = nullptr);
+GroupSet make_triple_groups(const bs_layout &A, const bs_layout &B, const bs_layout &C,
+                            const std::vector<uint8_t> *cmask = nullptr);
+// C blocks of shard `rank` out of `world`: every populated C block weighted by
+// its flops (sum over its triples of d_i d_k d_j), dealt largest first onto
+// the least loaded shard (ties: lowest shard), so every rank computes the same
+// partition on its own.  Returns a mask over C blocks.
+std::vector<uint8_t> shard_mask(const bs_layout &A, const bs_layout &B, const bs_layout &C, int rank, int world);
 void group_triples(const GroupSet &gs, std::vector<int64_t> *ptr, std::vector<int32_t> *out);
 // With materialize = false only what the cost model reads is produced: the
 // tile tasks (unsorted) and the executed flops; the tail list, its
 // descriptors and queues are left empty.  The planner costs every candidate
 // that way and materializes the chosen one.
 void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize = true);
-double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm, int64_t pack_bytes, int launches);
+double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm, int64_t pack_bytes, int launches,
+                     int64_t zero_bytes);
+
+// Forward: the BF16 model reads the plan's per-CTA lists.
+double model_bf16_us(const bs_plan &P, const PlanModel &pm);
 
 // Host description of one TMA tensor map of the BF16 path (encoded per call
 // with the caller's base pointer, then cached while the pointers stay the same).
@@ -68,6 +97,8 @@ struct MapDesc {
 
 struct bs_plan {
   int32_t dtype = BS_F64;
+  int32_t shard_rank = 0, shard_world = 1;   // this plan computes shard shard_rank of shard_world
+  std::vector<uint8_t> cmask;                // C blocks of the shard (empty: every block)
   bs_plan_options opts{};
   bs_layout A, B, C;
   bs_layout A_pk, B_pk;
@@ -86,6 +117,7 @@ struct bs_plan {
   std::vector<bs::Bf16Stage> bstages; // K stages in execution order, CTA after CTA
   std::vector<bs::MapDesc> maps;
   std::vector<unsigned char> map_bytes;   // encoded maps (128 bytes each)
+  std::vector<int16_t> sm_map;            // dense SM index per hardware SM identifier (FP64 tail queues)
   const void *maps_a_ptr = nullptr, *maps_b_ptr = nullptr;
   // device state
   int device = -1;
@@ -99,8 +131,6 @@ struct bs_plan {
   bs::KSeg *d_ksegs = nullptr;
   int32_t *d_tail = nullptr;
   bs::TailDesc *d_tdesc = nullptr;
-  int32_t *d_tq_ptr = nullptr;
-  int32_t *d_tq_items = nullptr;
   size_t counter_bytes = 256;
   bs::PackCopy *d_pack = nullptr;
   bs::ZeroBlock *d_zero = nullptr;
@@ -111,6 +141,10 @@ struct bs_plan {
   void *d_ws_a = nullptr, *d_ws_b = nullptr;
   uint32_t *d_counter = nullptr;
   int32_t *d_status = nullptr;
+  // phase events of bs_contract when profiling: before the gather, after it,
+  // after the zero fill, after the grouped kernel
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  bool ev_recorded = false;
   // staging for bs_contract_host
   void *d_host_a = nullptr, *d_host_b = nullptr, *d_host_c = nullptr;
   bs_plan_stats stats{};

@@ -163,7 +163,20 @@ typedef struct bs_plan_options {
                                  groups of one padded shape run as one batched call (uni20 design
                                  note "block coalescing", Open questions: bucketing near-same
                                  shapes by padding); padded rows, columns and K add only zeros */
-  int32_t reserved[5];
+  int32_t profile;            /* 1: bs_contract records CUDA events around each of its phases (gather,
+                                 zero fill, grouped kernel) on the caller's stream; read them with
+                                 bs_plan_profile.  0 (default): no events */
+  int32_t reserved[4];
+  /* further cost-model constants, also <= 0 for the built-in value (bs_calibration_apply fills
+     them from a measurement on the device) */
+  double t_fixed_us;          /* event-timed cost of a bs_contract whose kernel has almost no work */
+  double fp64_tail_gflops;    /* executed-flop rate of the lane-packed tail path, one view per group */
+  double fp64_general_gflops; /* the same for tail groups of several views (segment walk) */
+  double pack_fixed_us;       /* fixed cost of the gather launch */
+  double zero_gbs;            /* bandwidth of the zero fill that precedes atomic scatter */
+  double bf16_stage_us;       /* BF16 kernel: time per 64-deep K stage of a CTA's list */
+  double bf16_tile_us;        /* BF16 kernel: time per 128 x 256 output tile (epilogue) */
+  double reserved2[4];
 } bs_plan_options;
 
 enum { BS_DEBUG_WITHHOLD_COPY = 1, BS_DEBUG_MERGE_UNCHECKED = 2 };
@@ -214,10 +227,48 @@ bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype,
 bs_status bs_plan_create_into(const bs_layout *A, const bs_layout *B, const bs_layout *C, int32_t dtype,
                               const bs_plan_options *opts, bs_plan **out);
 
+/* One shard of the contraction for `world` GPUs (or processes), each running
+ * its own plan with no exchange of partial results: every populated C block is
+ * an independent unit (its value needs no other C block), so the C blocks are
+ * dealt largest first by flops onto the least loaded of `world` shards, and
+ * the plan of shard `rank` computes exactly its blocks (uni20 design note
+ * "block coalescing", "One mechanism, three payoffs": the same groups that
+ * cut launches are the units of distribution).  Every rank computes the same
+ * partition on its own.  C's layout is the whole structural product, so the
+ * shards agree on every offset; a shard writes only its own C blocks and
+ * reads only the A and B blocks their triples use (listed by
+ * bs_plan_operand_blocks, so a caller whose operands are distributed can
+ * gather just those).  The statistics count the shard only.  world = 1 is
+ * bs_plan_create.  INVALID_ARG unless 0 <= rank < world. */
+bs_status bs_plan_create_shard(const bs_layout *A, const bs_layout *B, int32_t dtype, const bs_plan_options *opts,
+                               int32_t rank, int32_t world, bs_plan **out);
+
+/* Blocks of operand 0 (A), 1 (B) or 2 (C) that the plan reads (A, B) or
+ * writes (C), as indices into that layout's block table in storage order
+ * (bs_layout_blocks; C's layout is bs_plan_c_layout), ascending.  Call with
+ * out = NULL for the count in *n. */
+bs_status bs_plan_operand_blocks(const bs_plan *plan, int32_t operand, int64_t *n, int32_t *out);
+
 /* C's layout, owned by the plan (valid until bs_plan_destroy). */
 const bs_layout *bs_plan_c_layout(const bs_plan *plan);
 
 bs_status bs_plan_stats_get(const bs_plan *plan, bs_plan_stats *out);
+
+/* Phase times of the plan's last bs_contract, for a plan built with
+ * opts->profile = 1: milliseconds between CUDA events recorded on the call's
+ * stream before and after the gather, the zero fill and the grouped kernel
+ * (0 for a phase the plan does not have), and their sum.  Waits for the last
+ * event.  INVALID_ARG when the plan does not profile or has not run. */
+typedef struct bs_phase_times {
+  double gather_ms;
+  double zero_ms;
+  double kernel_ms;
+  double total_ms;
+  int64_t gather_bytes;   /* bytes the gather reads plus writes (2 x packed bytes) */
+  int64_t reserved[3];
+} bs_phase_times;
+
+bs_status bs_plan_profile(bs_plan *plan, bs_phase_times *out);
 
 /* Group table for inspection: for each group g, out[g*8 + 0..7] =
  * {axis (1 contraction, 2 free, 3 none), M, N, K, m_segments, k_segments,
@@ -293,6 +344,11 @@ bs_status bs_contract_uncoalesced(bs_plan *plan, const void *A, const void *B, v
  *     that first call before any stream capture begins.
  *   - Every call shares the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race; order them on one stream.
+ *   - The tables are copied from the plan's host memory (ordinary pageable
+ *     memory), so a call may wait for earlier work on `stream` before it
+ *     returns, and the plan must stay alive until the call's work is done.
+ *   - A host_only plan built while a device is current is dealt for that
+ *     device's SM count; the grid is the one bs_contract would launch.
  *   - The FP64 kernel has no device waits, so there is no device status to read. */
 #define BS_NOALLOC_SCRATCH_BYTES (16u << 20)
 bs_status bs_contract_noalloc(const bs_plan *plan, const void *A, const void *B, void *C, void *stream);
@@ -311,13 +367,33 @@ const char *bs_status_string(bs_status status);
  * print; this call measures them with small probe kernels on `stream`
  * (allocating and freeing about 2 GiB of scratch) and synchronizes. */
 typedef struct bs_calibration {
-  double fp64_gflops;               /* FP64 FMA rate, every lane of every warp active */
+  double fp64_gflops;               /* FP64 FMA rate, every lane of every warp active (best probe shape) */
   double fp64_gflops_quarter_warp;  /* the same with 8 of 32 lanes active (useful flops) */
   double launch_us;                 /* back-to-back empty-kernel launch interval */
   double copy_gbs;                  /* device copy bandwidth, read + write bytes */
   int32_t sm_count;
-  int32_t reserved[7];
+  int32_t sm_id_bound;              /* 1 + the largest hardware SM identifier in use (> sm_count when
+                                       the identifiers skip values) */
+  double fp64_sm_mhz;               /* SM clock during the best FMA probe (cycle / global-time stamps) */
+  double fp64_flop_per_clk_sm;      /* FMA flops per SM clock at that rate */
+  double fp64_dmma_gflops;          /* FP64 matrix instruction (mma.sync m8n8k4) rate */
+  double dmma_flop_per_clk_sm;      /* its flops per SM clock */
+  /* cost-model constants, measured by running the library's own kernels on
+   * small synthetic structures (L2 flushed before every run, medians): */
+  double t_fixed_us;                /* bs_contract of a one-triple plan, event to event */
+  double tile_gflops;               /* tile path: useful rate on one dense 768^3 FP64 group */
+  double tail_gflops;               /* tail path, one view per group: executed flops / time */
+  double general_gflops;            /* tail path, several views per group */
+  double pack_gbs;                  /* gather kernel: 2 x packed bytes / time */
+  double pack_fixed_us;             /* gather kernel: time of a small gather */
+  double zero_gbs;                  /* zero fill: bytes / time */
+  double bf16_stage_us;             /* BF16 kernel: time per K stage, from one long dense group */
+  double bf16_tile_us;              /* BF16 kernel: time per output tile, from many short groups */
+  double reserved[7];
 } bs_calibration;
+
+/* Copy the cost-model constants of a calibration into planner options. */
+void bs_calibration_apply(const bs_calibration *cal, bs_plan_options *opts);
 
 bs_status bs_calibrate(bs_calibration *out, void *stream);
 

@@ -25,7 +25,7 @@ def _json_lines(out: str):
 
 def test_reference_arm_prints_one_line():
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3",
-                        "--cpu-workers", "2"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+                        "--cpu-workers", "2", "--config", "2"], cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
@@ -40,7 +40,8 @@ def test_reference_arm_under_torchrun_two_ranks():
     port = _free_port()
     r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
                         "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
-                        "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-workers", "2"],
+                        "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-workers", "2",
+                        "--config", "1"],
                        cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)

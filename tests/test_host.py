@@ -344,3 +344,57 @@ def test_random_structures_plan_exactly_and_hole_free(seed):
         assert P.check_groups() == (0, -1)
         assert P.c_layout.nelems == pr.lc.nelems
         assert np.array_equal(lib_blocks_by_rc(P.c_layout), pr.lc.blocks())
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("bucket", [0, 1])
+def test_auto_plan_costs_candidates_like_forced_plans(cfg, bucket):
+    """The AUTO planner costs every (axis, pack) candidate without listing its tail
+    outputs; a plan forced onto one candidate lists it in full.  Both must give the
+    same modelled time, and the AUTO plan's groups and triples must be the chosen
+    candidate's."""
+    w = bsgen.get(cfg)
+    if w.dtype == "bf16":
+        pytest.skip("the BF16 path has no axis or pack candidates to cost")
+    if cfg == 5 and bucket:
+        pytest.skip("one bucket setting is enough on the largest workload")
+    auto, _, _ = host_plan(w, bucket_pad=bucket)
+    sa = auto.stats()
+    forced = {}
+    for axis in (bs.AXIS_CONTRACTION, bs.AXIS_FREE):
+        for pack in (bs.PACK_NEVER, bs.PACK_ALWAYS):
+            P, _, _ = host_plan(w, axis_policy=axis, pack_policy=pack, bucket_pad=bucket)
+            forced[(axis, pack)] = P
+    chosen = (sa["axis"], bs.PACK_ALWAYS if (sa["packed_a"] or sa["packed_b"]) else bs.PACK_NEVER)
+    fc = forced[chosen]
+    sf = fc.stats()
+    assert sf["model_us"] == pytest.approx(sa["model_us"], rel=1e-12)
+    assert sf["executed_flops"] == pytest.approx(sa["executed_flops"], rel=1e-12)
+    assert sf["tasks"] == sa["tasks"] and sf["groups"] == sa["groups"]
+    others = [P.stats()["model_us"] for key, P in forced.items() if key != chosen]
+    assert min(others) == pytest.approx(sa["model_us_alt"], rel=1e-12)
+    assert all(sa["model_us"] <= o for o in others)
+    pa, ta = auto.triples()
+    pf, tf = fc.triples()
+    assert np.array_equal(pa, pf) and np.array_equal(ta, tf)
+    assert np.array_equal(auto.groups(), fc.groups())
+
+
+def test_host_allocation_fault_injection_returns_oom(monkeypatch):
+    """BS_FAULT_INJECT=alloc makes the host allocations of layout and plan
+    construction fail: the calls return BS_ERR_OOM and leave nothing behind, and
+    the same calls succeed again once the variable is gone."""
+    w = bsgen.config1()
+    A = bs.Layout(w.rows, w.inner, w.rule_a, w.layout_a, 8)
+    B = bs.Layout(w.inner, w.cols, w.rule_b, w.layout_b, 8)
+    monkeypatch.setenv("BS_FAULT_INJECT", "alloc")
+    with pytest.raises(bs.BsError) as e:
+        bs.Layout(w.rows, w.inner, w.rule_a, w.layout_a, 8)
+    assert e.value.code == 4
+    for _ in range(3):
+        with pytest.raises(bs.BsError) as e:
+            bs.Plan(A, B, bs.F64, host_only=1)
+        assert e.value.code == 4
+    monkeypatch.delenv("BS_FAULT_INJECT")
+    P = bs.Plan(A, B, bs.F64, host_only=1)
+    assert P.stats()["triples"] == 71

@@ -68,14 +68,24 @@ def test_noalloc_matches_contract_on_two_calls(name, make, lay, opts):
         assert rel.max() <= TOL["f64"], f"call {call}: worst per-block relative error {rel.max():.3e}"
 
 
+def _small_device_buffers(dtype):
+    """Real device buffers for the refusal tests: the call must refuse before it
+    touches them, but if a check ever regressed it would only read and write
+    these few valid bytes."""
+    return tuple(torch.zeros(64, dtype=dtype, device="cuda") for _ in range(3))
+
+
 def test_noalloc_rejects_a_plan_larger_than_its_array():
     w = bsgen.config5()
     A = bs.Layout(w.rows, w.inner, w.rule_a, w.layout_a, 8)
     B = bs.Layout(w.inner, w.cols, w.rule_b, w.layout_b, 8)
     host = bs.Plan(A, B, bs.F64, c_layout_flags=w.layout_c, host_only=1)
+    a, b, c = _small_device_buffers(torch.float64)
     with pytest.raises(bs.BsError) as e:
-        bs.contract_noalloc(host, 1 << 20, 1 << 20, 1 << 20)     # refused before anything is enqueued
+        bs.contract_noalloc(host, a, b, c)     # refused before anything is enqueued
     assert e.value.code == 9
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(c).item() == 0
 
 
 def test_noalloc_refuses_bf16_plans():
@@ -83,6 +93,9 @@ def test_noalloc_refuses_bf16_plans():
     A = bs.Layout(w.rows, w.inner, w.rule_a, w.layout_a, 2)
     B = bs.Layout(w.inner, w.cols, w.rule_b, w.layout_b, 2)
     host = bs.Plan(A, B, bs.BF16_F32, c_layout_flags=w.layout_c, host_only=1)
+    a, b, c = _small_device_buffers(torch.float32)
     with pytest.raises(bs.BsError) as e:
-        bs.contract_noalloc(host, 1 << 20, 1 << 20, 1 << 20)
+        bs.contract_noalloc(host, a, b, c)
     assert e.value.code == 3
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(c).item() == 0
