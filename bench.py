@@ -607,11 +607,20 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-workers", type=int, default=0, help="oracle worker processes (0: every core)")
     ap.add_argument("--skip-calib", action="store_true", help="skip the probe kernels (profiling runs)")
+    ap.add_argument("--gather-only", action="store_true",
+                    help="only time the gather kernel on the block-row layouts (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.gather_only:
+        import torch
+
+        import block_sparse_tensor_gb300 as bs
+        torch.cuda.set_device(0)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        print(json.dumps(gather_record(bs, torch, flush, torch.cuda.current_stream(), measured_peaks())), flush=True)
     else:
         run_gpu(args)
 

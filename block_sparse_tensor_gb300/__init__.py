@@ -35,7 +35,7 @@ EXPORTED = ["bs_layout_create", "bs_layout_query", "bs_layout_blocks", "bs_layou
             "bs_contract_uncoalesced", "bs_plan_last_device_error", "bs_plan_destroy",
             "bs_status_string", "bs_version", "bs_calibrate", "bs_contract_noalloc",
             "bs_plan_check_groups", "bs_plan_create_into", "bs_plan_profile", "bs_plan_create_shard",
-            "bs_plan_operand_blocks", "bs_calibration_apply"]
+            "bs_plan_operand_blocks", "bs_calibration_apply", "bs_contract_checked"]
 
 
 class BsError(RuntimeError):
@@ -66,11 +66,12 @@ class PlanOptions(ctypes.Structure):
                 ("t_segment_us", ctypes.c_double), ("pack_gbs", ctypes.c_double),
                 ("fp64_gflops", ctypes.c_double), ("atomic_penalty", ctypes.c_double),
                 ("wait_timeout_ms", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
-                ("bucket_pad", ctypes.c_int32), ("profile", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4),
+                ("bucket_pad", ctypes.c_int32), ("profile", ctypes.c_int32), ("tail_split_k", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3),
                 ("t_fixed_us", ctypes.c_double), ("fp64_tail_gflops", ctypes.c_double),
                 ("fp64_general_gflops", ctypes.c_double), ("pack_fixed_us", ctypes.c_double),
                 ("zero_gbs", ctypes.c_double), ("bf16_stage_us", ctypes.c_double), ("bf16_tile_us", ctypes.c_double),
-                ("reserved2", ctypes.c_double * 4)]
+                ("tile_k0", ctypes.c_double), ("reserved2", ctypes.c_double * 3)]
 
 
 class PlanStats(ctypes.Structure):
@@ -96,7 +97,8 @@ class Calibration(ctypes.Structure):
                 ("dmma_flop_per_clk_sm", ctypes.c_double), ("t_fixed_us", ctypes.c_double),
                 ("tile_gflops", ctypes.c_double), ("tail_gflops", ctypes.c_double), ("general_gflops", ctypes.c_double),
                 ("pack_gbs", ctypes.c_double), ("pack_fixed_us", ctypes.c_double), ("zero_gbs", ctypes.c_double),
-                ("bf16_stage_us", ctypes.c_double), ("bf16_tile_us", ctypes.c_double), ("reserved", ctypes.c_double * 7)]
+                ("bf16_stage_us", ctypes.c_double), ("bf16_tile_us", ctypes.c_double), ("tile_k0", ctypes.c_double),
+                ("atomic_factor", ctypes.c_double), ("reserved", ctypes.c_double * 5)]
 
 
 def _load(path: str = LIB_PATH):
@@ -131,6 +133,7 @@ def _load(path: str = LIB_PATH):
         "bs_plan_create_shard": (st, [P, P, i32, P, i32, i32, P]),
         "bs_plan_operand_blocks": (st, [P, i32, P, P]),
         "bs_calibration_apply": (None, [P, P]),
+        "bs_contract_checked": (st, [P, P, i64, P, i64, P, i64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -334,6 +337,15 @@ def contract(plan: Plan, A, B, C, stream=None):
     _check(lib.bs_contract(plan.h, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "bs_contract")
 
 
+def contract_checked(plan: Plan, A, B, C, nA=None, nB=None, nC=None, stream=None):
+    """bs_contract_checked: every access tested against the buffers' element counts
+    (default: the tensors' own numel).  A violation reads as BS_ERR_DEVICE from
+    last_device_error, or is raised at once when the host finds it."""
+    n = lambda x, v: int(v) if v is not None else int(x.numel())  # noqa: E731
+    _check(lib.bs_contract_checked(plan.h, _ptr(A), n(A, nA), _ptr(B), n(B, nB), _ptr(C), n(C, nC), _stream(stream)),
+           "bs_contract_checked")
+
+
 def contract_host(plan: Plan, A, B, C, stream=None):
     """C = A B on host buffers (numpy arrays or CPU tensors; pinned is fastest); synchronous."""
     _check(lib.bs_contract_host(plan.h, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "bs_contract_host")
@@ -375,7 +387,8 @@ def calibrated_options(cal: dict) -> dict:
     o = plan_options()
     lib.bs_calibration_apply(ctypes.byref(c), ctypes.byref(o))
     names = ("t_launch_us", "t_task_us", "t_segment_us", "pack_gbs", "fp64_gflops", "atomic_penalty", "t_fixed_us",
-             "fp64_tail_gflops", "fp64_general_gflops", "pack_fixed_us", "zero_gbs", "bf16_stage_us", "bf16_tile_us")
+             "fp64_tail_gflops", "fp64_general_gflops", "pack_fixed_us", "zero_gbs", "bf16_stage_us", "bf16_tile_us",
+             "tile_k0")
     return {n: getattr(o, n) for n in names if getattr(o, n) > 0}
 
 

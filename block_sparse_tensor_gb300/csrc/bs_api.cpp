@@ -343,7 +343,9 @@ struct Candidate {
 
 }  // namespace
 
-static bs_status contract_kernel(bs_plan *P, const void *Ause, const void *Buse, void *C, cudaStream_t s);
+static bs_status contract_kernel(bs_plan *P, const void *Ause, const void *Buse, void *C, cudaStream_t s,
+                                 const int64_t *sizes);
+static bs_status contract_impl(bs_plan *P, const void *A, const void *B, void *C, void *stream, const int64_t *sizes);
 
 extern "C" {
 
@@ -499,11 +501,13 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
     if (o.zero_gbs > 0) pm.zero_gbs = o.zero_gbs;
     if (o.bf16_stage_us > 0) pm.bf16_stage_us = o.bf16_stage_us;
     if (o.bf16_tile_us > 0) pm.bf16_tile_us = o.bf16_tile_us;
+    if (o.tile_k0 > 0) pm.tile_k0 = o.tile_k0;
     if (o.bucket_pad < 0 || o.bucket_pad > 1 || o.profile < 0 || o.profile > 1) {
       delete P;
       return BS_ERR_INVALID_ARG;
     }
     pm.bucket_pad = o.bucket_pad == 1;
+    pm.tail_split_k = o.tail_split_k > 0 ? o.tail_split_k : 0;
     if (!o.host_only) {
       int dev = 0, major = 0, minor = 0;
       if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -536,6 +540,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
                     : (o.host_only && P->device < 0) ? 3
                                                       : std::max(1, fp64_max_ctas_per_sm(false));
     pm.parallel_ctas = P->sm_count * cps;
+    P->parallel_ctas = pm.parallel_ctas;
     pm.sms = P->sm_count;
 
     const bool sorted_pack = true;
@@ -631,8 +636,11 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
           break;
         }
         if (std::getenv("BS_LOG"))
-          std::fprintf(stderr, "[bs] candidate axis=%d pack=%d groups=%zu tasks=%zu model=%.1f us (group %.1f ms, tile %.1f ms)\n",
-                       c.ax, (int)c.pk, c.gs.groups.size(), c.ts.tasks.size(), c.us, c.ms_group, c.ms_tile);
+          std::fprintf(stderr,
+                       "[bs] candidate axis=%d pack=%d groups=%zu tasks=%zu model=%.1f us (group %.1f ms, tile %.1f ms) "
+                       "executed tile %.4g tail %.4g general %.4g, costliest tile task %.4g tail task %.4g\n",
+                       c.ax, (int)c.pk, c.gs.groups.size(), c.ts.tasks.size(), c.us, c.ms_group, c.ms_tile,
+                       c.ts.exec_tile, c.ts.exec_tail, c.ts.exec_general, c.ts.max_tile_task, c.ts.max_tail_task);
         cands.push_back({c.ax, c.pk, c.us});
         if (c.us < best) {
           best = c.us;
@@ -792,6 +800,8 @@ void bs_calibration_apply(const bs_calibration *c, bs_plan_options *o) {
   set(c->zero_gbs, &o->zero_gbs);
   set(c->bf16_stage_us, &o->bf16_stage_us);
   set(c->bf16_tile_us, &o->bf16_tile_us);
+  set(c->tile_k0, &o->tile_k0);
+  set(c->atomic_factor, &o->atomic_penalty);
 }
 
 bs_status bs_plan_create_shard(const bs_layout *A, const bs_layout *B, int32_t dtype, const bs_plan_options *opts,
@@ -975,6 +985,25 @@ bs_status bs_plan_check_groups(const bs_plan *P, int64_t *bad_group) {
 }
 
 bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *stream) {
+  return contract_impl(P, A, B, C, stream, nullptr);
+}
+
+bs_status bs_contract_checked(bs_plan *P, const void *A, int64_t nA, const void *B, int64_t nB, void *C, int64_t nC,
+                              void *stream) {
+  if (nA < 0 || nB < 0 || nC < 0) return BS_ERR_INVALID_ARG;
+  const int64_t sizes[3] = {nA, nB, nC};
+  return contract_impl(P, A, B, C, stream, sizes);
+}
+
+}  // extern "C"
+
+// The element range [first, last] a strided view covers, against a buffer of n elements.
+static bool view_inside(int64_t off, int64_t rows, int64_t cols, int64_t ld, int64_t n) {
+  if (rows <= 0 || cols <= 0) return true;
+  return off >= 0 && off + (rows - 1) * ld + cols <= n;
+}
+
+static bs_status contract_impl(bs_plan *P, const void *A, const void *B, void *C, void *stream, const int64_t *sizes) {
   if (!P) return BS_ERR_INVALID_ARG;
   if (P->opts.host_only) return BS_ERR_INVALID_ARG;
   if (P->C.nelems == 0) return BS_OK;
@@ -982,6 +1011,24 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
   cudaStream_t s = (cudaStream_t)stream;
   const void *Ause = P->pack_a ? P->d_ws_a : A;
   const void *Buse = P->pack_b ? P->d_ws_b : B;
+  if (sizes) {
+    // what the host can check before anything is enqueued: the gather's reads,
+    // the zero fill's writes and the BF16 tensor maps' views
+    for (size_t t = 0; t < P->pack_copies.size(); ++t) {
+      const PackCopy &c = P->pack_copies[t];
+      const bool of_a = (int32_t)t < P->pack_copies_a;
+      if (!view_inside(c.src, c.rows, c.cols, c.src_ld, sizes[of_a ? 0 : 1])) return BS_ERR_DEVICE;
+    }
+    for (const auto &z : P->zero_blocks)
+      if (!view_inside(z.off, z.rows, z.cols, z.ld, sizes[2])) return BS_ERR_DEVICE;
+    for (const auto &m : P->maps) {
+      const int64_t n = m.operand == 0 ? (P->pack_a ? P->A_pk.nelems : sizes[0]) : (P->pack_b ? P->B_pk.nelems : sizes[1]);
+      if (!view_inside(m.off, m.outer, m.inner, m.ld, n)) return BS_ERR_DEVICE;
+    }
+    if (P->dtype == BS_BF16_F32)
+      for (const auto &t : P->btasks)
+        if (!view_inside(t.c_off, t.m, t.n, t.ldc, sizes[2])) return BS_ERR_DEVICE;
+  }
   const bool prof = P->opts.profile != 0;
   if (prof) {
     for (auto &e : P->ev)
@@ -1005,7 +1052,7 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
   if (!P->zero_blocks.empty())
     BS_CUDA(launch_zero(C, P->dtype == BS_F64 ? 8 : 4, P->d_zero, (int)P->zero_blocks.size(), P->sm_count * 4, s));
   if (prof) BS_CUDA(cudaEventRecord(P->ev[2], s));
-  bs_status st = contract_kernel(P, Ause, Buse, C, s);
+  bs_status st = contract_kernel(P, Ause, Buse, C, s, sizes);
   if (st == BS_OK && prof) {
     BS_CUDA(cudaEventRecord(P->ev[3], s));
     P->ev_recorded = true;
@@ -1013,9 +1060,8 @@ bs_status bs_contract(bs_plan *P, const void *A, const void *B, void *C, void *s
   return st;
 }
 
-}  // extern "C"
-
-static bs_status contract_kernel(bs_plan *P, const void *Ause, const void *Buse, void *C, cudaStream_t s) {
+static bs_status contract_kernel(bs_plan *P, const void *Ause, const void *Buse, void *C, cudaStream_t s,
+                                 const int64_t *sizes) {
   if (P->dtype == BS_F64) {
     if (P->ts.tasks.empty() && P->ts.tail_elems.empty()) return BS_OK;
     Fp64Params p{};
@@ -1032,6 +1078,12 @@ static bs_status contract_kernel(bs_plan *P, const void *Ause, const void *Buse,
     p.ntail = (int32_t)(P->ts.tail_elems.size() / 2);
     p.nct = (int32_t)((p.ntail + kThreads - 1) / kThreads);
     fill_queue_params(&p, P->ts.tq_ptr, P->sm_map);
+    if (sizes) {   // the checked instance: every operand load and C store against these counts
+      p.check = 1;
+      p.nA = P->pack_a ? P->A_pk.nelems : sizes[0];
+      p.nB = P->pack_b ? P->B_pk.nelems : sizes[1];
+      p.nC = sizes[2];
+    }
     p.counter = P->d_counter;
     p.status = P->d_status;
     BS_CUDA(launch_fp64_grouped(p, P->grid, s));

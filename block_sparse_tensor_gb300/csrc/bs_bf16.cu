@@ -36,7 +36,13 @@ namespace bs {
 
 namespace {
 
-constexpr int kStages = 4;
+#ifndef BS_BF16_STAGES
+#define BS_BF16_STAGES 4
+#endif
+#ifndef BS_BF16_EPI_WARPS
+#define BS_BF16_EPI_WARPS 8
+#endif
+constexpr int kStages = BS_BF16_STAGES;
 constexpr int kBM = 128;                          // rows of the accumulator (UMMA M)
 constexpr int kBK = 64;                           // K per stage (one 128-byte swizzle row of BF16)
 constexpr int kATileBytes = kBM * kBK * 2;        // 16 KB: 128 rows of A
@@ -44,7 +50,8 @@ constexpr int kBChunkBytes = 64 * kBK * 2;        // one 64-column N chunk of B:
 constexpr int kBTileBytes = 4 * kBChunkBytes;     // BN up to 256
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kTmemCols = 512;                    // two 256-column FP32 accumulator slots
-constexpr int kEpiWarps = 8;                      // two epilogue warps per TMEM lane quarter
+constexpr int kEpiWarps = BS_BF16_EPI_WARPS;      // epilogue warps, a multiple of 4 (one group per TMEM lane quarter)
+static_assert(kEpiWarps % 4 == 0, "epilogue warps per lane quarter");
 constexpr int kThreadsBf16 = 64 + 32 * kEpiWarps;
 constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x 32 FP32 columns per epilogue warp
 constexpr int kTaskCache = 16;                    // head of this CTA's task list, in shared memory
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
     // of four 128-byte row segments per instruction, masked at the group edge.
     const int quarter = warp & 3;
     const int ew = warp - 2;
-    const int grp = ew >> 2;                  // 0 or 1: which 32-column chunks
+    const int grp = ew >> 2;                  // which 32-column chunks: grp, grp + kEpiWarps/4, ...
     unsigned char *stg = epi_base + (size_t)ew * kEpiBufBytes;
     int slot = 0;
     uint32_t tf0 = 0, tf1 = 0;   // tfull phase per slot
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       if (row0 < T.m) {
         const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(slot * 256);
         float *cbase = p.C + T.c_off;
-        for (int c0 = 32 * grp; c0 < T.bn; c0 += 64) {
+        for (int c0 = 32 * grp; c0 < T.bn; c0 += 32 * (kEpiWarps / 4)) {
           float v[32];
           tmem_ld32(trow + c0, v);
           unsigned char *mine = stg + lane * 128;

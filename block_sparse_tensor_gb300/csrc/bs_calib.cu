@@ -14,6 +14,8 @@
 #include <algorithm>
 #include <chrono>
 #include <cmath>
+#include <cstdio>
+#include <cstdlib>
 #include <vector>
 
 #include "bs_plan.h"
@@ -142,7 +144,9 @@ CalStruct gaussian(int32_t h, double peak, double width) {
 struct CalRun {
   double us = 0;            // median event-to-event time of bs_contract
   double gather_ms = 0, zero_ms = 0;
-  double exec_tile = 0, exec_tail = 0, exec_general = 0;
+  double exec_tile = 0, exec_tail = 0, exec_general = 0, slots = 0;
+  double mtask = 0, mslots = 0, par = 1;   // costliest tile task: flops, slots; resident CTAs
+  double c_bytes = 0;       // populated C bytes
   bs_plan_stats st{};
   int64_t stages_max = 0, tiles_max = 0;   // BF16: the busiest CTA's stages and tiles
 };
@@ -150,7 +154,7 @@ struct CalRun {
 // Build the structure's layouts and plan, run bs_contract `reps` times with
 // L2 emptied before each (a write over `flush`), and report medians.
 bs_status cal_run(const CalStruct &cs, bs_plan_options o, void *flush, size_t flush_bytes, cudaStream_t s,
-                  cudaEvent_t e0, cudaEvent_t e1, int reps, CalRun *out) {
+                  cudaEvent_t e0, cudaEvent_t e1, int reps, CalRun *out, bool phases = false) {
   bs_axis_desc ax[3];
   for (int a = 0; a < 3; ++a) ax[a] = {(int32_t)cs.q[a].size(), cs.q[a].data(), nullptr, cs.d[a].data()};
   const bs_rule rule{-cs.band, cs.band, 0};
@@ -162,7 +166,7 @@ bs_status cal_run(const CalStruct &cs, bs_plan_options o, void *flush, size_t fl
   if (st == BS_OK) st = bs_layout_create(&ax[1], &ax[2], &rule, cs.flags[1], eb, &B);
   o.c_layout_flags = cs.flags[2];
   o.host_only = 0;
-  o.profile = 1;
+  o.profile = phases ? 1 : 0;   // phase events cost time of their own: only where a phase is measured
   if (st == BS_OK) st = bs_plan_create(A, B, cs.dtype, &o, &P);
   if (st == BS_OK) {
     const size_t na = (size_t)std::max<int64_t>(A->nelems, 8) * eb, nb = (size_t)std::max<int64_t>(B->nelems, 8) * eb;
@@ -186,7 +190,7 @@ bs_status cal_run(const CalStruct &cs, bs_plan_options o, void *flush, size_t fl
     float ms = 0;
     cudaEventElapsedTime(&ms, e0, e1);
     bs_phase_times ph{};
-    bs_plan_profile(P, &ph);
+    if (phases) bs_plan_profile(P, &ph);
     if (r >= 2) {   // two warm-up runs
       t.push_back(ms * 1e3);
       g.push_back(ph.gather_ms);
@@ -206,11 +210,23 @@ bs_status cal_run(const CalStruct &cs, bs_plan_options o, void *flush, size_t fl
     out->exec_tile = P->ts.exec_tile;
     out->exec_tail = P->ts.exec_tail;
     out->exec_general = P->ts.exec_general;
+    out->slots = P->ts.tile_slots;
+    out->mtask = P->ts.max_tile_task;
+    out->mslots = (double)P->ts.max_tile_slots;
+    out->par = std::max(1, P->parallel_ctas);
+    for (const auto &b : P->C.blocks) out->c_bytes += (double)b.rows * b.cols * ec;
     out->st = P->stats;
     for (const auto &c : P->bctas) {
       out->stages_max = std::max<int64_t>(out->stages_max, c.stage_count);
       out->tiles_max = std::max<int64_t>(out->tiles_max, c.task_count);
     }
+    if (std::getenv("BS_LOG"))
+      std::fprintf(stderr,
+                   "[bs] calibration run: %d sectors x %d, axis %d, packed %d, groups %lld, tasks %lld: %.2f us "
+                   "(gather %.2f us, zero %.2f us), executed tile %.3g tail %.3g general %.3g\n",
+                   (int)cs.q[0].size(), cs.d[0].empty() ? 0 : cs.d[0][0], out->st.axis, out->st.packed_a,
+                   (long long)out->st.groups, (long long)out->st.tasks, out->us, out->gather_ms * 1e3,
+                   out->zero_ms * 1e3, out->exec_tile, out->exec_tail, out->exec_general);
   }
   cudaFree(da);
   cudaFree(db);
@@ -221,7 +237,8 @@ bs_status cal_run(const CalStruct &cs, bs_plan_options o, void *flush, size_t fl
   return st;
 }
 
-// The cost-model constants of the planner, each from the run that isolates it.
+// The cost-model constants of the planner, each from the run that isolates it
+// (forced axis and gather policies, so each run takes the path it measures).
 bs_status calibrate_model(bs_calibration *out, cudaStream_t s) {
   const size_t flush_bytes = (size_t)256 << 20;
   void *flush = nullptr;
@@ -231,69 +248,126 @@ bs_status calibrate_model(bs_calibration *out, cudaStream_t s) {
   cudaEventCreate(&e1);
   bs_plan_options o;
   bs_plan_options_default(&o);
+  bs_plan_options oc = o;   // contraction axis, zero copy
+  oc.axis_policy = BS_AXIS_CONTRACTION;
+  oc.pack_policy = BS_PACK_NEVER;
+  bs_plan_options of = oc;  // free axis, zero copy
+  of.axis_policy = BS_AXIS_FREE;
+  bs_plan_options op = oc;  // contraction axis, gathered operands
+  op.pack_policy = BS_PACK_ALWAYS;
   bs_status st = BS_OK;
+  auto run = [&](const CalStruct &cs, const bs_plan_options &opt, int reps, CalRun *r, bool phases = false) {
+    return cal_run(cs, opt, flush, flush_bytes, s, e0, e1, reps, r, phases);
+  };
   do {
-    CalRun one, tile, tail, general, pack_small, pack_big, zero_big, bone, bdeep, bwide;
+    CalRun one, tile, tile_short, tail, general, tail_free, pack_small, pack_big, zero_big, bone, bdeep, bwide;
     // a contraction with almost no work: launch, first-task chain, exit
-    if ((st = cal_run(cube(1, 1), o, flush, flush_bytes, s, e0, e1, 20, &one)) != BS_OK) break;
+    if ((st = run(cube(1, 1), oc, 20, &one)) != BS_OK) break;
     out->t_fixed_us = one.us;
-    // one dense 768^3 group: the tile path
-    if ((st = cal_run(cube(1, 768), o, flush, flush_bytes, s, e0, e1, 5, &tile)) != BS_OK) break;
-    out->tile_gflops = tile.exec_tile / std::max(1e-3, tile.us - one.us) / 1e3;
-    // the 31-charge tail (every group one view): the lane-packed tail path
+    // tile path at long K: one dense 1536^3 group (its rate; k0 is fitted below)
+    if ((st = run(cube(1, 1536), oc, 5, &tile)) != BS_OK) break;
+    // tail path, one view per group: the 31-charge tail structure, contraction axis
     CalStruct g31 = gaussian(15, 64.0, 50.0);
-    if ((st = cal_run(g31, o, flush, flush_bytes, s, e0, e1, 20, &tail)) != BS_OK) break;
+    if ((st = run(g31, oc, 20, &tail)) != BS_OK) break;
     out->tail_gflops = (tail.exec_tail + tail.exec_general) / std::max(1e-3, tail.us - one.us) / 1e3;
-    // the same with block-row operands, contraction axis, no gather: several views per group
+    // several views per group: the same with block-row operands, contraction axis, no gather
     CalStruct g31b = g31;
     g31b.flags[0] = g31b.flags[1] = BS_LAYOUT_BLOCKROW;
-    bs_plan_options og = o;
-    og.axis_policy = BS_AXIS_CONTRACTION;
-    og.pack_policy = BS_PACK_NEVER;
-    if ((st = cal_run(g31b, og, flush, flush_bytes, s, e0, e1, 20, &general)) != BS_OK) break;
+    if ((st = run(g31b, oc, 20, &general)) != BS_OK) break;
     const double t_single = general.exec_tail / (out->tail_gflops * 1e3);
     out->general_gflops = general.exec_general / std::max(1e-3, general.us - one.us - t_single) / 1e3;
+    // the zero fill before atomic scatter: the large structure on the free axis
+    if ((st = run(gaussian(20, 384.0, 60.0), of, 5, &zero_big, true)) != BS_OK) break;
+    out->zero_gbs = zero_big.zero_ms > 0 ? zero_big.c_bytes / (zero_big.zero_ms * 1e-3) / 1e9 : 0.0;
+    // atomic stores: 1000 small sectors (charges spread over -30..30, dims
+    // 1..8) on the free axis, where every group is a tail group stored with
+    // atomics, against the time its flops take at the plain rates
+    CalStruct small;
+    for (int a = 0; a < 3; ++a)
+      for (int32_t t = 0; t < 1000; ++t) {
+        small.q[a].push_back((t * 37 + a * 11) % 61 - 30);
+        small.d[a].push_back(1 + (t * 7 + a * 3) % 8);
+      }
+    small.band = 1;
+    if ((st = run(small, of, 10, &tail_free)) != BS_OK) break;
+    {
+      const double plain = tail_free.exec_tail / (out->tail_gflops * 1e3) + tail_free.exec_general / (out->general_gflops * 1e3);
+      const double t = tail_free.us - one.us - out->launch_us - tail_free.c_bytes / (out->zero_gbs * 1e3);
+      out->atomic_factor = t > 0 ? std::min(1.0, plain / t) : 1.0;
+    }
+    // short-K tile tasks: the tail structure on the free axis (rows of up to
+    // three sectors stacked, K = one inner sector of at most 64), where the
+    // per-chunk staging shows; k0 is the extra K a task costs so that the
+    // model meets this run, and the long-K rate is refitted with it
+    if ((st = run(g31, of, 20, &tile_short)) != BS_OK) break;
+    {
+      PlanModel pm;
+      pm.parallel_ctas = std::max(1, (int)tile.par);
+      pm.t_launch_us = out->launch_us;
+      pm.zero_gbs = out->zero_gbs;
+      pm.tail_gflops = out->tail_gflops;
+      pm.general_gflops = out->general_gflops;
+      pm.atomic_penalty = out->atomic_factor;
+      auto model_tile = [&](const CalRun &r, double rate, double k0) {
+        const double rt = rate * 1e3, per_cta = rt / std::max(1, (int)r.par);
+        const double work = (r.exec_tile + 2.0 * k0 * r.slots) / rt;
+        const double drain = r.mtask > 0 ? (r.mtask + 2.0 * k0 * r.mslots) / per_cta : 0.0;
+        const double tail = (r.exec_tail / (pm.tail_gflops * 1e3) + r.exec_general / (pm.general_gflops * 1e3)) /
+                            (r.st.axis == BS_AXIS_CONTRACTION ? 1.0 : pm.atomic_penalty);
+        return work + std::max(drain, tail);
+      };
+      double rate = tile.exec_tile / std::max(1e-3, tile.us - one.us) / 1e3, k0 = 0;
+      const double t_short = tile_short.us - one.us - out->launch_us - tile_short.c_bytes / (out->zero_gbs * 1e3);
+      for (int it = 0; it < 4; ++it) {
+        // k0 by bisection on the short-K run (the model grows with k0) ...
+        double lo = 0, hi = 1024;
+        if (model_tile(tile_short, rate, 0) >= t_short) hi = 0;
+        for (int b = 0; b < 40 && hi > 0; ++b) {
+          const double mid = 0.5 * (lo + hi);
+          if (model_tile(tile_short, rate, mid) < t_short) lo = mid;
+          else hi = mid;
+        }
+        k0 = 0.5 * (lo + hi);
+        // ... then the long-K rate with that k0 (the model falls as the rate grows)
+        double rl = 10, rh = 1e5;
+        for (int b = 0; b < 60; ++b) {
+          const double mid = std::sqrt(rl * rh);
+          if (model_tile(tile, mid, k0) > tile.us - one.us) rl = mid;
+          else rh = mid;
+        }
+        rate = std::sqrt(rl * rh);
+      }
+      out->tile_gflops = rate;
+      out->tile_k0 = k0;
+    }
     // the gather, small (its fixed cost) and large (its bandwidth)
-    bs_plan_options op = og;
-    op.pack_policy = BS_PACK_ALWAYS;
-    if ((st = cal_run(g31b, op, flush, flush_bytes, s, e0, e1, 20, &pack_small)) != BS_OK) break;
+    if ((st = run(g31b, op, 20, &pack_small, true)) != BS_OK) break;
     out->pack_fixed_us = pack_small.gather_ms * 1e3;
     CalStruct g41b = gaussian(20, 384.0, 60.0);
     g41b.flags[0] = g41b.flags[1] = g41b.flags[2] = BS_LAYOUT_BLOCKROW;
-    if ((st = cal_run(g41b, op, flush, flush_bytes, s, e0, e1, 5, &pack_big)) != BS_OK) break;
-    out->pack_gbs = 2.0 * pack_big.st.packed_bytes / std::max(1e-3, pack_big.gather_ms * 1e3 - out->pack_fixed_us) / 1e3;
-    // the zero fill before atomic scatter, on the large structure's C
-    bs_plan_options oz = o;
-    oz.axis_policy = BS_AXIS_FREE;
-    oz.pack_policy = BS_PACK_NEVER;
-    if ((st = cal_run(gaussian(20, 384.0, 60.0), oz, flush, flush_bytes, s, e0, e1, 5, &zero_big)) != BS_OK) break;
+    if ((st = run(g41b, op, 5, &pack_big, true)) != BS_OK) break;
+    // gather time = fixed + 2 x packed bytes / bandwidth, through both points
+    out->pack_gbs = 2.0 * (double)(pack_big.st.packed_bytes - pack_small.st.packed_bytes) /
+                    std::max(1e-3, (pack_big.gather_ms - pack_small.gather_ms) * 1e3) / 1e3;
+    out->pack_fixed_us = std::max(0.0, pack_small.gather_ms * 1e3 -
+                                            2.0 * pack_small.st.packed_bytes / (out->pack_gbs * 1e3));
     // BF16: one 128 x 256 tile with one stage (fixed cost), one deep group
     // (stages), many shallow groups (tiles)
     CalStruct b1 = cube(1, 64, BS_BF16_F32);
     b1.d[2].assign(1, 256);
     b1.d[0].assign(1, 128);
-    if ((st = cal_run(b1, o, flush, flush_bytes, s, e0, e1, 20, &bone)) != BS_OK) break;
+    if ((st = run(b1, o, 20, &bone)) != BS_OK) break;
     CalStruct b2 = cube(1, 256, BS_BF16_F32);
-    b2.d[0].assign(1, 128);
-    b2.d[1].assign(1, 8192);   // 128 stages of 64 on one CTA
-    if ((st = cal_run(b2, o, flush, flush_bytes, s, e0, e1, 10, &bdeep)) != BS_OK) break;
+    b2.d[0].assign(1, 128 * 152);
+    b2.d[1].assign(1, 4096);   // 64 stages of 64 on every CTA at once
+    if ((st = run(b2, o, 10, &bdeep)) != BS_OK) break;
     out->bf16_stage_us = std::max(0.0, bdeep.us - bone.us) / std::max<int64_t>(1, bdeep.stages_max - 1);
     CalStruct b3 = cube(1, 64, BS_BF16_F32);
     b3.d[0].assign(1, 128 * 152 * 8);   // eight 128 x 256 tiles of one stage on every CTA
     b3.d[2].assign(1, 256);
-    if ((st = cal_run(b3, o, flush, flush_bytes, s, e0, e1, 10, &bwide)) != BS_OK) break;
+    if ((st = run(b3, o, 10, &bwide)) != BS_OK) break;
     out->bf16_tile_us = std::max(0.0, bwide.us - bone.us - (bwide.stages_max - 1) * out->bf16_stage_us) /
                         std::max<int64_t>(1, bwide.tiles_max - 1);
-    // zero fill bandwidth: its populated C bytes over the measured phase
-    {
-      int64_t cbytes = 0;
-      CalStruct zs = gaussian(20, 384.0, 60.0);
-      // C of the free-axis plan: every populated block of the product, 8 bytes each
-      for (size_t i = 0; i < zs.q[0].size(); ++i)
-        for (size_t j = 0; j < zs.q[2].size(); ++j)
-          if (std::abs(zs.q[0][i] - zs.q[2][j]) <= 2) cbytes += (int64_t)zs.d[0][i] * zs.d[2][j] * 8;
-      out->zero_gbs = zero_big.zero_ms > 0 ? cbytes / (zero_big.zero_ms * 1e-3) / 1e9 : 0.0;
-    }
   } while (false);
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);

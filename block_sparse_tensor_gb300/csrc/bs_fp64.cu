@@ -47,6 +47,36 @@ __device__ __forceinline__ int find_kseg(const KSeg *ks, int n, int k) {
   return lo;
 }
 
+// Operand loads and C stores.  The checked instance (bs_contract_checked)
+// tests every index against the buffer's element count first: an access
+// outside is skipped (a load reads zero) and the status word records it.
+__device__ __forceinline__ void flag_bounds(const Fp64Params &p) { atomicExch(p.status, (int32_t)DS_BOUNDS); }
+
+template <bool kCheck>
+__device__ __forceinline__ double ld_op(const Fp64Params &p, const double *base, int64_t n, const double *ptr) {
+  if (kCheck) {
+    const int64_t i = ptr - base;
+    if (i < 0 || i >= n) {
+      flag_bounds(p);
+      return 0.0;
+    }
+  }
+  return __ldg(ptr);
+}
+
+template <bool kCheck>
+__device__ __forceinline__ void st_c(const Fp64Params &p, double *ptr, double v, bool atomic) {
+  if (kCheck) {
+    const int64_t i = ptr - p.C;
+    if (i < 0 || i >= p.nC) {
+      flag_bounds(p);
+      return;
+    }
+  }
+  if (atomic) atomicAdd(ptr, v);
+  else *ptr = v;
+}
+
 struct TileSmem {
   double As[kKC][kTileMaxDim + 1];   // A chunk, inner index major: As[kk][row]
   double Bs[kKC][kTileMaxDim + 1];   // B chunk: Bs[kk][col]
@@ -59,6 +89,7 @@ struct TileSmem {
   int task;
 };
 
+template <bool kCheck>
 __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
   const int tid = threadIdx.x;
   const Group G = p.groups[T.g];
@@ -98,11 +129,11 @@ __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
     __syncthreads();
     for (int idx = tid; idx < tm * kn; idx += kThreads) {
       const int r = idx / kn, kk = idx - r * kn;
-      sm.As[kk][r] = __ldg(p.A + sm.rowA[r] + sm.kA[kk] + sm.rowL[r] * sm.kL[kk]);
+      sm.As[kk][r] = ld_op<kCheck>(p, p.A, p.nA, p.A + sm.rowA[r] + sm.kA[kk] + sm.rowL[r] * sm.kL[kk]);
     }
     for (int idx = tid; idx < kn * tn; idx += kThreads) {
       const int kk = idx / tn, c = idx - kk * tn;
-      sm.Bs[kk][c] = __ldg(p.B + sm.kB[kk] + c);
+      sm.Bs[kk][c] = ld_op<kCheck>(p, p.B, p.nB, p.B + sm.kB[kk] + c);
     }
     __syncthreads();
     if (active) {
@@ -118,9 +149,7 @@ __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
 #pragma unroll
   for (int u = 0; u < kElemsPerThread; ++u) {
     if (orow[u] < 0) continue;
-    double *dst = p.C + sm.rowC[orow[u]] + T.n0 + ocol[u];
-    if (atomic) atomicAdd(dst, acc[u]);
-    else *dst = acc[u];
+    st_c<kCheck>(p, p.C + sm.rowC[orow[u]] + T.n0 + ocol[u], acc[u], atomic);
   }
 }
 
@@ -129,10 +158,13 @@ __device__ void run_tile(const Fp64Params &p, const Task &T, TileSmem &sm) {
 // When every lane's group is one view (the usual case with panel layouts) the
 // loop is unrolled with six accumulators; otherwise each lane walks its
 // group's views, switching view on its own.
+template <bool kCheck>
 __device__ void run_tail_warp(const Fp64Params &p, int w) {
   const int lane = threadIdx.x & 31;
   const int e = w * 32 + lane;
-  const int2 el = e < p.ntail ? p.tail_elems[e] : make_int2(p.tail_elems[w * 32].x, kTailPad);
+  int2 el = e < p.ntail ? p.tail_elems[e] : make_int2(p.tail_elems[w * 32].x, kTailPad);
+  const bool hi = (el.x & kTailHi) != 0;   // second half of a split output's K
+  el.x &= ~kTailHi;
   const bool ok = el.y != kTailPad;   // a padding entry holds no output
   const int r = el.y >> 16, c = el.y & 0xFFFF;
   // single-segment groups: addressing resolved at plan time, one table load
@@ -143,10 +175,15 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
   bool live = ok;   // this lane owns a real output (padded lanes of a bucket do not)
   if (__all_sync(0xFFFFFFFFu, D.k > 0)) {
     live = ok && r < D.m && c < D.n;
-    const int kg = live ? D.k : 0;   // steps that load data
-    const int kmax = __reduce_max_sync(0xFFFFFFFFu, ok ? (unsigned)D.kpad : 0u);   // steps run
-    const double *ap = p.A + D.a0 + (int64_t)r * D.as;
-    const double *bp = p.B + D.b0 + c;
+    // a split output's lanes sum K steps [0, kh) and [kh, kpad); others [0, kpad)
+    const bool split = __any_sync(0xFFFFFFFFu, hi);   // split groups fill whole warps
+    const int kh = split ? (D.kpad + 1) >> 1 : 0;
+    const int k0 = hi ? kh : 0;
+    const int kend = split && !hi ? kh : D.kpad;
+    const int kg = live ? max(0, min(D.k, kend) - k0) : 0;   // steps that load data
+    const int kmax = __reduce_max_sync(0xFFFFFFFFu, ok ? (unsigned)(kend - k0) : 0u);   // steps run
+    const double *ap = p.A + D.a0 + (int64_t)r * D.as + k0;
+    const double *bp = p.B + D.b0 + (int64_t)k0 * D.ldb + c;
     const int64_t ldb = D.ldb;
     cofs = D.c0 + (int64_t)r * D.ldc + c;
     flags = D.flags;
@@ -164,15 +201,19 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
       double x[U], y[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        x[u] = it + u < kg ? __ldg(ap + it + u) : 0.0;
-        y[u] = it + u < kg ? __ldg(bp + (it + u) * ldb) : 0.0;
+        x[u] = it + u < kg ? ld_op<kCheck>(p, p.A, p.nA, ap + it + u) : 0.0;
+        y[u] = it + u < kg ? ld_op<kCheck>(p, p.B, p.nB, bp + (it + u) * ldb) : 0.0;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) a[u] = fma(x[u], y[u], a[u]);
     }
     for (; it < kmax; ++it)
-      if (it < kg) a[0] = fma(__ldg(ap + it), __ldg(bp + it * ldb), a[0]);
+      if (it < kg) a[0] = fma(ld_op<kCheck>(p, p.A, p.nA, ap + it), ld_op<kCheck>(p, p.B, p.nB, bp + it * ldb), a[0]);
     acc = ((a[0] + a[1]) + (a[2] + a[3])) + (a[4] + a[5]);
+    if (split) {   // the second half's partial sum joins its output on the lane 16 below
+      acc += __shfl_down_sync(0xFFFFFFFFu, acc, 16);
+      live = live && !hi;
+    }
   } else {
     // general path: walk the group's row and inner segments
     const Group G = p.groups[el.x];
@@ -199,7 +240,7 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
           ldb = k.ldb;
           rem = k.klen;
         }
-        acc = fma(__ldg(ap), __ldg(bp), acc);
+        acc = fma(ld_op<kCheck>(p, p.A, p.nA, ap), ld_op<kCheck>(p, p.B, p.nB, bp), acc);
         ++ap;
         bp += ldb;
         --rem;
@@ -207,9 +248,7 @@ __device__ void run_tail_warp(const Fp64Params &p, int w) {
     }
   }
   if (live) {
-    double *d = p.C + cofs;
-    if (flags & GF_ATOMIC) atomicAdd(d, acc);
-    else *d = acc;
+    st_c<kCheck>(p, p.C + cofs, acc, (flags & GF_ATOMIC) != 0);
   }
 }
 
@@ -227,7 +266,7 @@ __device__ __forceinline__ int home_queue(const Fp64Params &p) {
 // tasks, whose shared-memory staging wants the most resident warps, and three
 // for plans made only of tail tasks, which measure faster with fewer, quicker
 // CTAs sharing each SM.
-template <int kMinCtas>
+template <int kMinCtas, bool kCheck>
 __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Params p) {
   __shared__ TileSmem sm;
   // tile tasks, one CTA each, longest first
@@ -237,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Pa
     const int t = sm.task;
     __syncthreads();
     if (t >= p.ntasks) break;
-    run_tile(p, p.tasks[t], sm);
+    run_tile<kCheck>(p, p.tasks[t], sm);
   }
   // Then the tail: CTA-sized tasks (kThreads consecutive outputs of the tail
   // list, so the 8 warps walk the same B rows through L1), dealt at plan time
@@ -288,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Pa
       __syncthreads();
       if (ct < 0) break;
       const int w = ct * (kThreads / 32) + warp;
-      if (w * 32 < p.ntail) run_tail_warp(p, w);
+      if (w * 32 < p.ntail) run_tail_warp<kCheck>(p, w);
     }
   }
   __syncthreads();
@@ -313,42 +352,57 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Pa
 
 // The gather: one warp per block copy, copies listed largest first at plan
 // time and dealt to the warps in turn (each warp fetches its next copy's
-// descriptor while it moves the current one).  No element index is divided:
-//   - a copy whose rows are contiguous in both buffers (ld = cols on both
-//     sides) is one flat range, moved 16 bytes per lane when both ends are
-//     16-byte aligned;
-//   - rows of at most 32 elements: each lane keeps one (row offset, column)
-//     pair for the whole copy, so a warp moves floor(32 / cols) rows a step;
-//   - wider rows: the lanes walk each row, 16 bytes at a time when every row
-//     of both views starts on a 16-byte boundary.
-template <class T, int kUnroll>
-__device__ __forceinline__ void copy_span(const T *__restrict__ s, T *__restrict__ d, int n, int lane, bool vec) {
-  constexpr int V = 16 / (int)sizeof(T);
-  int x0 = 0;
-  if (vec) {
-    const int nv = n / V;   // whole 16-byte units
-    const int4 *sv = (const int4 *)s;
-    int4 *dv = (int4 *)d;
-    int u = lane;
-    for (; u + 32 * (kUnroll - 1) < nv; u += 32 * kUnroll) {
-      int4 t[kUnroll];
+// descriptor while it moves the current one).  A copy is moved in 16-byte
+// units when both views allow it (every row start 16-byte aligned and whole
+// rows of units), else element by element.  The warp walks the copy's
+// (row, column) positions 32 at a time with four loads in flight per lane and
+// divides no index: rows of at most 32 units map each lane to one fixed
+// (row offset, column) pair, so a step covers floor(32 / cols) rows; wider
+// rows advance each lane's position by 32 columns, wrapping to the next row.
+template <class U>
+__device__ __forceinline__ void copy_2d(const U *__restrict__ src, int64_t sld, U *__restrict__ dst, int64_t dld,
+                                        int rows, int cols, int lane) {
+  constexpr int kU = 4;
+  if (cols <= 32) {
+    const int rpw = 32 / cols;
+    const int lr = lane / cols, lc = lane - lr * cols;
+    if (lr >= rpw) return;
+    const U *sp = src + lc;
+    U *dp = dst + lc;
+    int r = lr;
+    for (; r + (kU - 1) * rpw < rows; r += kU * rpw) {
+      U t[kU];
 #pragma unroll
-      for (int q = 0; q < kUnroll; ++q) t[q] = __ldg(sv + u + 32 * q);
+      for (int q = 0; q < kU; ++q) t[q] = __ldg(sp + (int64_t)(r + q * rpw) * sld);
 #pragma unroll
-      for (int q = 0; q < kUnroll; ++q) dv[u + 32 * q] = t[q];
+      for (int q = 0; q < kU; ++q) dp[(int64_t)(r + q * rpw) * dld] = t[q];
     }
-    for (; u < nv; u += 32) dv[u] = __ldg(sv + u);
-    x0 = nv * V;
+    for (; r < rows; r += rpw) dp[(int64_t)r * dld] = __ldg(sp + (int64_t)r * sld);
+    return;
   }
-  int x = x0 + lane;
-  for (; x + 32 * (kUnroll - 1) < n; x += 32 * kUnroll) {
-    T t[kUnroll];
+  // cols > 32: a step of 32 positions moves a lane at most into the next row
+  int r = 0, c = lane;
+  for (;;) {
+    int rr[kU], cc[kU];
 #pragma unroll
-    for (int q = 0; q < kUnroll; ++q) t[q] = __ldg(s + x + 32 * q);
+    for (int q = 0; q < kU; ++q) {
+      rr[q] = r;
+      cc[q] = c;
+      c += 32;
+      if (c >= cols) {
+        c -= cols;
+        ++r;
+      }
+    }
+    U t[kU];
 #pragma unroll
-    for (int q = 0; q < kUnroll; ++q) d[x + 32 * q] = t[q];
+    for (int q = 0; q < kU; ++q)
+      if (rr[q] < rows) t[q] = __ldg(src + (int64_t)rr[q] * sld + cc[q]);
+#pragma unroll
+    for (int q = 0; q < kU; ++q)
+      if (rr[q] < rows) dst[(int64_t)rr[q] * dld + cc[q]] = t[q];
+    if (rr[kU - 1] >= rows || r >= rows) break;
   }
-  for (; x < n; x += 32) d[x] = __ldg(s + x);
 }
 
 template <class T>
@@ -366,30 +420,17 @@ __global__ void pack_kernel(PackParams a, PackParams b, int32_t ntotal) {
     const T *src = (const T *)pp.src + cur.src;
     T *dst = (T *)pp.dst + cur.dst;
     const bool base16 = (((uintptr_t)pp.src | (uintptr_t)pp.dst) & 15u) == 0;
-    if (cur.src_ld == cur.cols && cur.dst_ld == cur.cols) {
-      const bool vec = base16 && ((cur.src | cur.dst) % V) == 0;
-      copy_span<T, 4>(src, dst, cur.rows * cur.cols, lane, vec);
-    } else if (cur.cols <= 32) {
-      const int rpw = 32 / cur.cols;
-      const int lr = lane / cur.cols, lc = lane - lr * cur.cols;
-      if (lr < rpw) {
-        const T *sp = src + lc;
-        T *dp = dst + lc;
-        int r = lr;
-        for (; r + 3 * rpw < cur.rows; r += 4 * rpw) {
-          T t[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) t[q] = __ldg(sp + (int64_t)(r + q * rpw) * cur.src_ld);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dp[(int64_t)(r + q * rpw) * cur.dst_ld] = t[q];
-        }
-        for (; r < cur.rows; r += rpw) dp[(int64_t)r * cur.dst_ld] = __ldg(sp + (int64_t)r * cur.src_ld);
-      }
-    } else {
-      const bool vec = base16 && ((cur.src | cur.dst | cur.src_ld | cur.dst_ld) % V) == 0;
-      for (int r = 0; r < cur.rows; ++r)
-        copy_span<T, 2>(src + (int64_t)r * cur.src_ld, dst + (int64_t)r * cur.dst_ld, cur.cols, lane, vec);
+    int64_t sld = cur.src_ld, dld = cur.dst_ld;
+    int rows = cur.rows, cols = cur.cols;
+    if (sld == cols && dld == cols) {   // contiguous on both sides: one flat row
+      cols = rows * cols;
+      rows = 1;
+      sld = dld = cols;
     }
+    if (base16 && ((cur.src | cur.dst | sld | dld | (int64_t)cols) % V) == 0)
+      copy_2d<int4>((const int4 *)src, sld / V, (int4 *)dst, dld / V, rows, cols / V, lane);
+    else
+      copy_2d<T>(src, sld, dst, dld, rows, cols, lane);
   }
 }
 
@@ -432,16 +473,21 @@ __global__ void control_bf16_kernel(const uint16_t *A, const uint16_t *B, float 
 }  // namespace
 
 cudaError_t launch_fp64_grouped(const Fp64Params &p, int grid, cudaStream_t s) {
-  if (p.ntasks > 0) fp64_grouped_kernel<4><<<grid, kThreads, 0, s>>>(p);
-  else fp64_grouped_kernel<3><<<grid, kThreads, 0, s>>>(p);
+  if (p.check) {
+    if (p.ntasks > 0) fp64_grouped_kernel<4, true><<<grid, kThreads, 0, s>>>(p);
+    else fp64_grouped_kernel<3, true><<<grid, kThreads, 0, s>>>(p);
+  } else {
+    if (p.ntasks > 0) fp64_grouped_kernel<4, false><<<grid, kThreads, 0, s>>>(p);
+    else fp64_grouped_kernel<3, false><<<grid, kThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
 int fp64_max_ctas_per_sm(bool tail_only) {
   int n = 0;
   const cudaError_t e = tail_only
-                            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp64_grouped_kernel<3>, kThreads, 0)
-                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp64_grouped_kernel<4>, kThreads, 0);
+                            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp64_grouped_kernel<3, false>, kThreads, 0)
+                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp64_grouped_kernel<4, false>, kThreads, 0);
   return e == cudaSuccess && n > 0 ? n : 1;
 }
 

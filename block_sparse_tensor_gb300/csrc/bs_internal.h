@@ -127,6 +127,9 @@ constexpr int kMaxQueues = 160;   // tail queues: one per SM, at most this many
 constexpr int kMaxSmIds = 256;    // hardware SM identifiers the parameter map covers
 // Tail-list entry that pads a tail task to kThreads outputs: no output.
 constexpr int32_t kTailPad = 0x7FFF7FFF;
+// Set in a tail entry's group field: the entry sums the second half of K of an
+// output whose first half the lane 16 below sums (a split group).
+constexpr int32_t kTailHi = 1 << 30;
 
 struct Fp64Params {
   const double *A;
@@ -145,6 +148,8 @@ struct Fp64Params {
   uint32_t *counter;   // [0] next tile task, [1] CTAs finished, [2] tail tasks taken;
                        // counter[64 + q]: next task of queue q.  All return to 0 at exit.
   int32_t *status;
+  int64_t nA, nB, nC;  // elements of the buffers read and written (the checked instance tests them)
+  int32_t check;       // 1: the checked instance
   int32_t nsm_ids;     // entries of sm_queue in use (0: take %smid modulo nq)
   // Kept in the parameters, so a CTA finds its first task without a memory load:
   int32_t qptr[kMaxQueues + 1];   // queue q holds tail tasks qptr[q] .. qptr[q+1]-1 (consecutive)

@@ -366,7 +366,8 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
   ts->tail_elems.clear();
   ts->tq_ptr.clear();
   ts->tdesc.clear();
-  ts->exec_tile = ts->exec_tail = ts->exec_general = ts->max_tail_task = 0;
+  ts->exec_tile = ts->exec_tail = ts->exec_general = ts->max_tail_task = ts->max_tile_task = ts->tile_slots = 0;
+  ts->max_tile_slots = 0;
   if (materialize) ts->tdesc.assign(gs.groups.size(), TailDesc{});
   std::vector<std::pair<double, Task>> costed;
   std::vector<int32_t> tails;
@@ -395,6 +396,11 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
         const double slots = (double)lanes((int64_t)t.tm * t.tn);
         exec += 2.0 * slots * G.k;
         ts->exec_tile += 2.0 * slots * G.k;
+        ts->tile_slots += slots;
+        if (2.0 * slots * G.k > ts->max_tile_task) {
+          ts->max_tile_task = 2.0 * slots * G.k;
+          ts->max_tile_slots = (int64_t)slots;
+        }
         costed.push_back({slots * G.k + pm.task_slots, t});
       }
   }
@@ -416,55 +422,90 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
     *np = pad ? pow2(G.n) : G.n;
     *kp = pad ? pow2(G.k) : G.k;
   };
+  // A group of one view whose K reaches tail_split_k runs each output on two
+  // lanes of one warp: lanes 0-15 sum the first half of K for 16 outputs,
+  // lanes 16-31 the second half for the same outputs, and one shuffle adds
+  // them.  Its warps then run half as long, which halves the longest tail
+  // tasks (they share an SM's pipe with the other CTAs for their whole life)
+  // and lets the plan-time dealing balance the SMs more finely.
+  auto split_of = [&](int32_t g, int32_t kp) {
+    const Group &G = gs.groups[g];
+    return pm.tail_split_k > 0 && G.rseg_count == 1 && G.kseg_count == 1 && kp >= pm.tail_split_k;
+  };
+  auto lane_k = [&](int32_t g) {
+    int32_t mp, np, kp;
+    padded(g, &mp, &np, &kp);
+    return split_of(g, kp) ? (kp + 1) / 2 : kp;
+  };
   std::stable_sort(tails.begin(), tails.end(), [&](int32_t a, int32_t b) {
-    int32_t ma, na, ka, mb, nb, kb;
-    padded(a, &ma, &na, &ka);
-    padded(b, &mb, &nb, &kb);
-    if (!pm.bucket_pad) return ka > kb;   // exact: by K only, as listed
+    const int32_t ka = lane_k(a), kb = lane_k(b);
+    if (!pm.bucket_pad) return ka > kb;   // exact: by K per lane only, as listed
+    int32_t ma, na, xa, mb, nb, xb;
+    padded(a, &ma, &na, &xa);
+    padded(b, &mb, &nb, &xb);
     return std::make_tuple(-ka, ma, na) < std::make_tuple(-kb, mb, nb);
   });
-  // The executed flops of the tail list without listing it: each warp of 32
-  // consecutive outputs runs its first output's K, and the outputs of the
-  // sorted groups follow one another.  Split by path: groups of one view
-  // (row and inner) take the unrolled loop, the others the segment walk.
-  {
+  // One walk over the sorted groups lays out the tail list: each warp of 32
+  // consecutive entries runs its first lane's K (the list runs longest K
+  // first); a split group starts on a warp boundary (the previous warp is
+  // padded with entries that hold no output) and takes one warp per 16 of its
+  // outputs.  The walk gives the executed flops split by path (groups of one
+  // view take the unrolled loop, the others the segment walk) and the cost
+  // of the first, costliest task; with `emit` it also writes the list.
+  std::vector<int32_t> elem_k;
+  auto walk = [&](bool emit) {
     int64_t off = 0;
-    for (int32_t g : tails) {
-      int32_t mp, np, kp;
-      padded(g, &mp, &np, &kp);
-      const int64_t end = off + (int64_t)mp * np;
-      const int64_t warps = (end + 31) / 32 - (off + 31) / 32;   // warp starts inside [off, end)
-      const double ex = 2.0 * 32.0 * kp * (double)warps;
-      const Group &G = gs.groups[g];
-      if (G.rseg_count == 1 && G.kseg_count == 1) ts->exec_tail += ex;
-      else ts->exec_general += ex;
-      off = end;
-    }
-  }
-  // The costliest tail task is the first one (the list runs longest K first):
-  // each of its warps runs its first output's K.
-  {
-    int64_t off = 0;
-    int wstart = 0;
-    for (int32_t g : tails) {
-      int32_t mp, np, kp;
-      padded(g, &mp, &np, &kp);
-      const int64_t end = off + (int64_t)mp * np;
-      while (wstart < kThreads && wstart < end) {
-        ts->max_tail_task += 2.0 * 32.0 * kp;
-        wstart += 32;
+    auto push = [&](int32_t g, int32_t rc, int32_t k) {
+      if (emit) {
+        ts->tail_elems.push_back(g);
+        ts->tail_elems.push_back(rc);
+        elem_k.push_back(k);
       }
-      off = end;
-      if (wstart >= kThreads) break;
+    };
+    auto count_warps = [&](int64_t from, int64_t to, int32_t k, bool single) {
+      const int64_t warps = (to + 31) / 32 - (from + 31) / 32;   // warp starts inside [from, to)
+      const double ex = 2.0 * 32.0 * k * (double)warps;
+      if (single) ts->exec_tail += ex;
+      else ts->exec_general += ex;
+      for (int64_t w = (from + 31) / 32 * 32; w < to && w < kThreads; w += 32) ts->max_tail_task += 2.0 * 32.0 * k;
+    };
+    for (int32_t g : tails) {
+      const Group &G = gs.groups[g];
+      int32_t mp, np, kp;
+      padded(g, &mp, &np, &kp);
+      const bool single = G.rseg_count == 1 && G.kseg_count == 1;
+      const int64_t nout = (int64_t)mp * np;
+      if (split_of(g, kp)) {
+        const int32_t lk = (kp + 1) / 2;
+        while (off % 32) {   // fill the previous warp
+          push(g, kTailPad, 0);
+          ++off;
+        }
+        for (int64_t c0 = 0; c0 < nout; c0 += 16)
+          for (int half = 0; half < 2; ++half)
+            for (int64_t e = c0; e < c0 + 16; ++e) {
+              const int32_t gg = half ? (g | kTailHi) : g;
+              if (e < nout) push(gg, (int32_t)(((e / np) << 16) | (e % np)), lk);
+              else push(gg, kTailPad, 0);
+            }
+        const int64_t end = off + (nout + 15) / 16 * 32;
+        count_warps(off, end, lk, true);
+        off = end;
+      } else {
+        for (int32_t r = 0; emit && r < mp; ++r)
+          for (int32_t c = 0; c < np; ++c) push(g, (r << 16) | c, kp);
+        count_warps(off, off + nout, kp, single);
+        off += nout;
+      }
     }
-  }
+  };
+  walk(!materialize ? false : true);
   if (!materialize) {
     exec += ts->exec_tail + ts->exec_general;
     for (auto &c : costed) ts->tasks.push_back(c.second);
     ts->executed_flops = exec;
     return;
   }
-  std::vector<int32_t> elem_k;
   for (int32_t g : tails) {
     const Group &G = gs.groups[g];
     int32_t mp, np, kp;
@@ -485,12 +526,6 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
       d.m = G.m;
       d.n = G.n;
     }
-    for (int32_t r = 0; r < mp; ++r)
-      for (int32_t c = 0; c < np; ++c) {
-        ts->tail_elems.push_back(g);
-        ts->tail_elems.push_back((r << 16) | c);
-        elem_k.push_back(kp);
-      }
   }
   // Tail tasks of kThreads outputs (one CTA, one output per thread): the 8
   // warps of a task hold consecutive outputs of the same group(s), so they
@@ -549,24 +584,31 @@ void tile_fp64(GroupSet &gs, const PlanModel &pm, TileSet *ts, bool materialize)
 
 double model_fp64_us(const GroupSet &gs, const TileSet &ts, const PlanModel &pm, int64_t pack_bytes, int launches,
                      int64_t zero_bytes) {
-  // Flop time of each path at its measured rate; the tail also cannot end
-  // before its costliest task has run at its share of one SM (the SM's CTAs
-  // split its FP64 pipe evenly).
-  const double sm_share_gflops = pm.tail_gflops / std::max(1, pm.parallel_ctas);
-  const double tail = std::max(ts.exec_tail / (pm.tail_gflops * 1e3) + ts.exec_general / (pm.general_gflops * 1e3),
-                               ts.max_tail_task / (sm_share_gflops * 1e3));
-  const double compute = ts.exec_tile / (pm.fp64_gflops * 1e3) + tail;
-  int64_t nseg = 0, natomic_elems = 0;
+  // Tile path: every task costs as if its K were K + tile_k0 (staging and
+  // synchronisation per chunk), and the launch cannot end before its
+  // costliest task has run at its CTA's share of one SM.
+  const double r_tile = pm.fp64_gflops * 1e3;   // flops per microsecond
+  const double tile = (ts.exec_tile + 2.0 * pm.tile_k0 * ts.tile_slots) / r_tile;
+  const double per_cta = r_tile / std::max(1, pm.parallel_ctas);
+  const double drain = ts.max_tile_task > 0 ? (ts.max_tile_task + 2.0 * pm.tile_k0 * ts.max_tile_slots) / per_cta : 0.0;
+  // (tile tasks run first, longest first; the last of them overlaps the tail
+  // work that the CTAs finishing earlier pick up)
+  // Tail path at its measured rates; groups stored with atomics (free axis,
+  // no coalescing) run at atomic_penalty of them.
+  bool atomic = false;
+  int64_t nseg = 0;
   for (const auto &g : gs.groups) {
     nseg += g.kseg_count + g.rseg_count;
-    if (g.flags & GF_ATOMIC) natomic_elems += (int64_t)g.m * g.n;
+    atomic |= (g.flags & GF_ATOMIC) != 0;
   }
+  const double f = atomic ? pm.atomic_penalty : 1.0;
+  const double tail = ts.exec_tail / (pm.tail_gflops * 1e3 * f) + ts.exec_general / (pm.general_gflops * 1e3 * f);
   const double par = std::max(1, pm.parallel_ctas);
   const double overhead = ((double)ts.tasks.size() * pm.t_task_us + (double)nseg * pm.t_segment_us) / par;
-  const double atomics = pm.atomic_penalty * natomic_elems * 8.0 / (pm.zero_gbs * 1e3);
   const double zero = zero_bytes > 0 ? (double)zero_bytes / (pm.zero_gbs * 1e3) : 0.0;
   const double pack = pack_bytes > 0 ? pm.pack_fixed_us + 2.0 * pack_bytes / (pm.pack_gbs * 1e3) : 0.0;
-  return pm.t_fixed_us + std::max(0, launches - 1) * pm.t_launch_us + compute + overhead + atomics + zero + pack;
+  return pm.t_fixed_us + std::max(0, launches - 1) * pm.t_launch_us + tile + std::max(drain, tail) + overhead + zero +
+         pack;
 }
 
 double model_bf16_us(const bs_plan &P, const PlanModel &pm) {

@@ -31,6 +31,9 @@ struct TileSet {
   // loop), tail groups of several views (the segment walk)
   double exec_tile = 0, exec_tail = 0, exec_general = 0;
   double max_tail_task = 0;   // executed flops of the costliest tail task
+  double max_tile_task = 0;   // executed flops of the costliest tile task
+  double tile_slots = 0;      // sum over tile tasks of their output slots (lanes)
+  int64_t max_tile_slots = 0; // output slots of the costliest tile task
 };
 
 // Cost model of one contraction (microseconds).  The defaults are this
@@ -38,22 +41,24 @@ struct TileSet {
 // device and bs_calibration_apply hands them to the planner.
 struct PlanModel {
   double t_launch_us = 2.0;      // each kernel of a contraction after the first
-  double t_task_us = 0.4;
-  double t_segment_us = 0.03;
+  double t_task_us = 0.0;        // extra fixed cost per task (none measured beyond the terms below)
+  double t_segment_us = 0.0;     // extra cost per view segment (likewise)
   double pack_gbs = 3700.0;
   double pack_fixed_us = 8.0;
-  double fp64_gflops = 1150.0;   // tile path, useful = executed
-  double tail_gflops = 900.0;    // tail path, one view per group, executed flops
-  double general_gflops = 300.0; // tail path, several views per group
+  double fp64_gflops = 1190.0;   // tile path at long K, useful = executed
+  double tile_k0 = 0.0;          // a tile task costs as if its K were K + tile_k0
+  double tail_gflops = 1000.0;   // tail path, one view per group, executed flops
+  double general_gflops = 500.0; // tail path, several views per group
   double zero_gbs = 3000.0;
   double t_fixed_us = 10.0;      // a contraction whose kernel has almost no work
-  double atomic_penalty = 0.5;
+  double atomic_penalty = 0.5;   // rate factor of tail groups stored with atomics
   double bf16_stage_us = 0.5;
   double bf16_tile_us = 2.8;
   double task_slots = 4096;   // LPT weight of a task's fixed cost, in lane-flop units
   int parallel_ctas = 456;
   int sms = 152;
   bool bucket_pad = false;    // pad single-segment tail groups to power-of-two shapes
+  int tail_split_k = 0;       // single-view tail groups of at least this K run each output on two lanes (0: never)
 };
 
 // `cmask` (indexed by C block, may be null): only the triples whose C block it
@@ -122,6 +127,7 @@ struct bs_plan {
   // device state
   int device = -1;
   int sm_count = 0;
+  int parallel_ctas = 0;   // resident CTAs the cost model assumed
   int grid = 0;
   void *d_tables = nullptr;
   size_t tables_bytes = 0;

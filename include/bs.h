@@ -150,7 +150,7 @@ typedef struct bs_plan_options {
   double t_segment_us;        /* extra cost of one zero-copy view segment inside a task */
   double pack_gbs;            /* achieved bandwidth of the gather kernel */
   double fp64_gflops;         /* sustained FP64 pipe rate of the grouped kernel */
-  double atomic_penalty;      /* relative cost of an atomic scatter store vs a plain store */
+  double atomic_penalty;      /* rate factor (0..1] of tail groups stored with atomics (free axis, none) */
   int32_t wait_timeout_ms;    /* limit of every device-side wait (BF16 path); <= 0: 2000 ms */
   int32_t debug_flags;        /* testing only, 0 in normal use: BS_DEBUG_WITHHOLD_COPY makes
                                  the BF16 producer skip its first copy so the consumer's bounded
@@ -166,7 +166,11 @@ typedef struct bs_plan_options {
   int32_t profile;            /* 1: bs_contract records CUDA events around each of its phases (gather,
                                  zero fill, grouped kernel) on the caller's stream; read them with
                                  bs_plan_profile.  0 (default): no events */
-  int32_t reserved[4];
+  int32_t tail_split_k;       /* FP64 tail: a group of one view whose K reaches this (> 0) runs
+                                 each output on two lanes, each summing half of K (halves the
+                                 longest tail tasks; measured no faster on the tail workload and
+                                 6% slower on the stress workload, so off by default); <= 0: never */
+  int32_t reserved[3];
   /* further cost-model constants, also <= 0 for the built-in value (bs_calibration_apply fills
      them from a measurement on the device) */
   double t_fixed_us;          /* event-timed cost of a bs_contract whose kernel has almost no work */
@@ -176,7 +180,8 @@ typedef struct bs_plan_options {
   double zero_gbs;            /* bandwidth of the zero fill that precedes atomic scatter */
   double bf16_stage_us;       /* BF16 kernel: time per 64-deep K stage of a CTA's list */
   double bf16_tile_us;        /* BF16 kernel: time per 128 x 256 output tile (epilogue) */
-  double reserved2[4];
+  double tile_k0;             /* FP64 tile path: a task costs as if its K were K + tile_k0 */
+  double reserved2[3];
 } bs_plan_options;
 
 enum { BS_DEBUG_WITHHOLD_COPY = 1, BS_DEBUG_MERGE_UNCHECKED = 2 };
@@ -306,6 +311,21 @@ bs_status bs_plan_check_groups(const bs_plan *plan, int64_t *bad_group);
  * on the device are reported by bs_plan_last_device_error. */
 bs_status bs_contract(bs_plan *plan, const void *A, const void *B, void *C, void *stream);
 
+/* bs_contract with every access checked against the caller's buffer sizes
+ * (a debugging aid, slower than bs_contract).  nA, nB and nC are the elements
+ * the A, B and C buffers hold.  Before anything is enqueued the host checks
+ * the views the gather reads, the C blocks the zero fill writes and, for a
+ * BF16 plan, every tensor map's view and every output tile against them, and
+ * returns BS_ERR_DEVICE on the first that does not fit.  An FP64 plan then
+ * runs a checked instance of its kernel: every load of A or B and every store
+ * of C is tested against the counts first; an access outside is skipped (a
+ * load reads zero) and the kernel records a bounds violation, which
+ * bs_plan_last_device_error reports as BS_ERR_DEVICE.  No access ever leaves
+ * the buffers, and a plan whose layouts fit its buffers trips nothing.
+ * INVALID_ARG for negative counts, otherwise as bs_contract. */
+bs_status bs_contract_checked(bs_plan *plan, const void *A, int64_t nA, const void *B, int64_t nB, void *C,
+                              int64_t nC, void *stream);
+
 /* The same contraction on HOST buffers: copies A and B to plan-owned device
  * buffers (allocated on first use), contracts into C_host (which must hold the
  * C layout's element count) and synchronizes the stream before returning.
@@ -381,7 +401,7 @@ typedef struct bs_calibration {
   /* cost-model constants, measured by running the library's own kernels on
    * small synthetic structures (L2 flushed before every run, medians): */
   double t_fixed_us;                /* bs_contract of a one-triple plan, event to event */
-  double tile_gflops;               /* tile path: useful rate on one dense 768^3 FP64 group */
+  double tile_gflops;               /* tile path at long K (one dense 1536^3 FP64 group) */
   double tail_gflops;               /* tail path, one view per group: executed flops / time */
   double general_gflops;            /* tail path, several views per group */
   double pack_gbs;                  /* gather kernel: 2 x packed bytes / time */
@@ -389,7 +409,9 @@ typedef struct bs_calibration {
   double zero_gbs;                  /* zero fill: bytes / time */
   double bf16_stage_us;             /* BF16 kernel: time per K stage, from one long dense group */
   double bf16_tile_us;              /* BF16 kernel: time per output tile, from many short groups */
-  double reserved[7];
+  double tile_k0;                   /* tile path: extra K steps a task costs (from a short-K group) */
+  double atomic_factor;             /* tail path: rate of atomically stored groups relative to plain ones */
+  double reserved[5];
 } bs_calibration;
 
 /* Copy the cost-model constants of a calibration into planner options. */

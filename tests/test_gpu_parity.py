@@ -401,3 +401,22 @@ def test_config4_blockrow_gather_path_every_block():
     r = Run(w, w.pack_layout_a, w.pack_layout_b, w.pack_layout_c)
     assert r.P.stats()["packed_a"] == 1
     compare_all(r, r.run())
+
+
+# ---------------------------------------------------------------- long-K tail outputs on two lanes
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("split_k", [2, 9, 0])
+def test_split_tail_outputs_integer_inputs_bit_exact(seed, split_k):
+    """Tail groups of one view whose K reaches tail_split_k run each output on two
+    lanes (each sums half of K, one shuffle adds them); integer inputs make the
+    result exact, split or not, padded buckets included."""
+    w = bsgen.tiny_random(300 + seed, values="int3", max_sectors=12, max_dim=17)
+    r = Run(w, *LAYOUTS[["panels", "mixed"][seed % 2]], axis_policy=bs.AXIS_CONTRACTION,
+            tail_split_k=split_k, bucket_pad=seed % 3 == 2)
+    compare(r, r.run(), exact=True)
+
+
+@pytest.mark.parametrize("split_k", [8, 64])
+def test_split_tail_outputs_tail_workload_every_block(split_k):
+    r = Run(bsgen.config2(), tail_split_k=split_k)
+    compare(r, r.run())

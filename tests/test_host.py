@@ -296,6 +296,9 @@ def test_bucket_padding_accounts_its_waste():
         assert sb["triples"] == se["triples"] and sb["groups"] == se["groups"]
         assert sb["useful_flops"] == se["useful_flops"]
         assert se["executed_flops"] < 1.001 * se["useful_flops"]
+        # splitting long-K outputs over two lanes pads only the last 16-output chunk of a group
+        split, _, _ = host_plan(w, axis_policy=axis, tail_split_k=64)
+        assert se["executed_flops"] < split.stats()["executed_flops"] < 1.01 * se["useful_flops"]
         assert sb["executed_flops"] > 1.5 * sb["useful_flops"]
         assert sb["tail_tasks"] > se["tail_tasks"]
         assert bk.check_groups() == (0, -1)
