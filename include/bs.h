@@ -103,7 +103,10 @@ typedef struct bs_block_info {
 } bs_block_info;
 
 /* Build the layout of a tensor over (rows x cols) whose populated blocks are
- * those the rule allows.  elem_bytes (2, 4 or 8) matters only for ALIGN16.
+ * those the rule allows (uni20 design note "block coalescing", "Expressed as
+ * strided views over shared storage": every block an (offset, leading
+ * dimension) view into one buffer; "Interleaved vs contiguous": the
+ * arrangement decides which blocks form one wider view).  elem_bytes (2, 4 or 8) matters only for ALIGN16.
  * Errors: INVALID_ARG (NULL, n < 0, dim < 1, z2 rule without parities, bad
  * flags or elem_bytes), OVERFLOW (element count beyond int64), OOM. */
 bs_status bs_layout_create(const bs_axis_desc *rows, const bs_axis_desc *cols, const bs_rule *rule,
@@ -210,7 +213,12 @@ typedef struct bs_plan_stats {
   double plan_ms;             /* host time spent in bs_plan_create */
 } bs_plan_stats;
 
-/* Build the contraction plan for C = A B.  A's column axis and B's row axis
+/* Build the contraction plan for C = A B (uni20 design note "block
+ * coalescing": Summary, the populated triples; "Why single-axis coalescing is
+ * hole-free", the contraction-axis and free-axis groups; "The crossover
+ * decides whether to coalesce" and "Interleaved vs contiguous", the cost model
+ * that picks the axis and whether to gather; "Coalescing is a plan-time
+ * transform", all of it done here once).  A's column axis and B's row axis
  * must be identical (same n, charges, parities, dims) or SHAPE_MISMATCH.
  * dtype fixes the element types; elem_bytes of the layouts must match it
  * (8 for F64; 2 for BF16 inputs).  C's layout is built by the plan over
@@ -301,7 +309,9 @@ bs_status bs_plan_triples(const bs_plan *plan, int64_t *ntriples, int64_t *ngrou
  * (may be NULL); -1 there when every group passes. */
 bs_status bs_plan_check_groups(const bs_plan *plan, int64_t *bad_group);
 
-/* Enqueue C = A B on `stream` and return at once.  A, B, C are device
+/* Enqueue C = A B on `stream` and return at once (uni20 design note "block
+ * coalescing", Summary: the plain sum over populated triples, run as few
+ * large launches instead of one per triple).  A, B, C are device
  * pointers to buffers laid out per the plan's A, B and C layouts; every
  * populated C element is overwritten; padding and absent blocks are not
  * touched.  A, B and C must not overlap.  Work: an optional gather, an optional
