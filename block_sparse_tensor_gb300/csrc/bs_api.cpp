@@ -1046,7 +1046,7 @@ static bs_status contract_impl(bs_plan *P, const void *A, const void *B, void *C
     PackParams pb = pp;
     pb.src = B;
     pb.dst = P->d_ws_b;
-    BS_CUDA(launch_pack2(pp, pb, (int32_t)P->pack_copies.size(), P->sm_count * 8, s));
+    BS_CUDA(launch_pack2(pp, pb, (int32_t)P->pack_copies.size(), P->sm_count, s));
   }
   if (prof) BS_CUDA(cudaEventRecord(P->ev[1], s));
   if (!P->zero_blocks.empty())

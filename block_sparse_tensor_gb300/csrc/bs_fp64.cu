@@ -21,6 +21,8 @@
 //     over the lanes.
 // Stores are plain for contraction-axis groups (each C block has one writer)
 // and atomic adds for free-axis groups (several k add into one C block).
+#include <algorithm>
+
 #include "bs_host.h"
 
 namespace bs {
@@ -491,8 +493,12 @@ int fp64_max_ctas_per_sm(bool tail_only) {
   return e == cudaSuccess && n > 0 ? n : 1;
 }
 
-cudaError_t launch_pack2(const PackParams &a, const PackParams &b, int32_t ntotal, int grid, cudaStream_t s) {
+cudaError_t launch_pack2(const PackParams &a, const PackParams &b, int32_t ntotal, int sms, cudaStream_t s) {
   if (ntotal <= 0) return cudaSuccess;
+  // eight CTAs per SM, about two waves at this kernel's occupancy: the copies
+  // are dealt to the warps in turn, and the second wave's warps pick up the
+  // shares of the first wave's slowest (measured faster than one wave)
+  int grid = std::max(1, sms) * 8;
   const int need = (ntotal + 7) / 8;   // one warp per copy, eight warps a CTA
   grid = grid < need ? grid : need;
   if (a.elem_bytes == 8) pack_kernel<double><<<grid, 256, 0, s>>>(a, b, ntotal);
