@@ -303,7 +303,7 @@ bs_status upload(bs_plan *P) {
   P->d_bstasks = (Bf16Task *)(b + o_bt);
   P->d_bstages = (Bf16Stage *)(b + o_bs);
   P->d_maps = (void *)(b + o_maps);
-  // counters and status word: zero once, kernels return them to zero
+  // status word and the two counter sets (initialised once the grid is known)
   void *cs = nullptr;
   P->counter_bytes = counter_bytes((int)std::max<size_t>(1, P->ts.tq_ptr.size()) - 1);
   BS_CUDA(cudaMalloc(&cs, P->counter_bytes));
@@ -315,6 +315,15 @@ bs_status upload(bs_plan *P) {
   if (P->pack_b) BS_CUDA(cudaMalloc(&P->d_ws_b, std::max<int64_t>(P->B_pk.nelems, 1) * eb));
   P->stats.workspace_bytes = (int64_t)total + 256 + (P->pack_a ? P->A_pk.nelems * eb : 0) +
                              (P->pack_b ? P->B_pk.nelems * eb : 0);
+  return BS_OK;
+}
+
+// Both counter sets and the status word of a plan back to zero; the next
+// launch uses set 0.
+bs_status init_counters(bs_plan *P) {
+  if (!P->d_counter) return BS_OK;
+  BS_CUDA(cudaMemset(P->d_counter, 0, P->counter_bytes));
+  P->counter_parity = 0;
   return BS_OK;
 }
 
@@ -769,6 +778,12 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
         P->grid = (int)std::max<int64_t>(1, std::min<int64_t>(work_items, (int64_t)P->sm_count * launch_cps));
       }
       else P->grid = std::max(1, (int)P->bctas.size());
+      st = init_counters(P);
+      if (st != BS_OK) {
+        free_device(P);
+        delete P;
+        return st;
+      }
     }
   } catch (const std::bad_alloc &) {
     free_device(P);
@@ -1084,9 +1099,23 @@ static bs_status contract_kernel(bs_plan *P, const void *Ause, const void *Buse,
       p.nB = P->pack_b ? P->B_pk.nelems : sizes[1];
       p.nC = sizes[2];
     }
-    p.counter = P->d_counter;
+    // Alternate launches use alternate counter sets, each launch preparing the
+    // other; a launch being captured into a graph (replayed with the same
+    // pointers) resets its own set at exit instead and leaves the parity.
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    BS_CUDA(cudaStreamIsCapturing(s, &capturing));
+    const bool captured = capturing != cudaStreamCaptureStatusNone;
+    {
+      const int nq = (int)std::max<size_t>(1, P->ts.tq_ptr.size()) - 1;   // as counter_bytes was sized
+      char *sets = (char *)P->d_counter + 256;
+      p.counter = (uint32_t *)(sets + (size_t)P->counter_parity * counter_set_bytes(nq));
+      p.counter_next =
+          captured ? nullptr : (uint32_t *)(sets + (size_t)(1 - P->counter_parity) * counter_set_bytes(nq));
+      p.reset_at_exit = captured ? 1 : 0;
+    }
     p.status = P->d_status;
     BS_CUDA(launch_fp64_grouped(p, P->grid, s));
+    if (!captured) P->counter_parity ^= 1;
   } else {
     if (((uintptr_t)Ause | (uintptr_t)Buse | (uintptr_t)C) % 16 != 0) return BS_ERR_MISALIGNED;
     if (P->btasks.empty()) return BS_OK;
@@ -1212,7 +1241,8 @@ bs_status bs_plan_last_device_error(bs_plan *P, void *stream) {
   if (v != 0) {
     BS_CUDA(cudaMemset(P->d_status, 0, sizeof v));
     // a kernel that stopped early may leave the work counters set
-    BS_CUDA(cudaMemset(P->d_counter, 0, P->counter_bytes));
+    bs_status st = init_counters(P);
+    if (st != BS_OK) return st;
   }
   if (v == DS_OK) return BS_OK;
   if (v == DS_TIMEOUT) return BS_ERR_TIMEOUT;

@@ -264,6 +264,15 @@ __device__ __forceinline__ int home_queue(const Fp64Params &p) {
   return idx % p.nq;
 }
 
+// A counter set as a launch finds it: every count at zero.
+__device__ __forceinline__ void init_counter_set(const Fp64Params &p, uint32_t *set) {
+  for (int q = threadIdx.x; q < p.nq; q += kThreads) atomicExch(&set[kQueueCounterBase + q], 0u);
+  if (threadIdx.x == 0) {
+    atomicExch(&set[0], 0u);
+    atomicExch(&set[2], 0u);
+  }
+}
+
 // Two instances: four CTAs per SM (64 registers a thread) for plans with tile
 // tasks, whose shared-memory staging wants the most resident warps, and three
 // for plans made only of tail tasks, which measure faster with fewer, quicker
@@ -271,6 +280,9 @@ __device__ __forceinline__ int home_queue(const Fp64Params &p) {
 template <int kMinCtas, bool kCheck>
 __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Params p) {
   __shared__ TileSmem sm;
+  // CTA 0 prepares the other counter set for the next launch (the set is idle
+  // during this one), so this launch's own set needs no reset at exit
+  if (blockIdx.x == 0 && p.counter_next) init_counter_set(p, p.counter_next);
   // tile tasks, one CTA each, longest first
   for (; p.ntasks > 0;) {
     if (threadIdx.x == 0) sm.task = (int)atomicAdd(&p.counter[0], 1u);
@@ -332,23 +344,21 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Pa
       if (w * 32 < p.ntail) run_tail_warp<kCheck>(p, w);
     }
   }
-  __syncthreads();
-  // The last CTA to leave returns the counters to zero for the next launch,
-  // all of its threads at once.  Every CTA has taken its final work index
-  // before it counts itself out.
-  if (threadIdx.x == 0) {
-    __threadfence();
-    sm.task = atomicAdd(&p.counter[1], 1u) == gridDim.x - 1 ? 1 : 0;
-  }
-  __syncthreads();
-  if (sm.task) {
-    for (int q = threadIdx.x; q < p.nq; q += kThreads) atomicExch(&p.counter[kQueueCounterBase + q], 0u);
+  if (p.reset_at_exit) {
+    // a replayed launch finds its own set as it found it: the last CTA to
+    // leave (every CTA has taken its final work index before it counts
+    // itself out) writes the initial values back
+    __syncthreads();
     if (threadIdx.x == 0) {
-      atomicExch(&p.counter[0], 0u);
-      atomicExch(&p.counter[2], 0u);
+      __threadfence();
+      sm.task = atomicAdd(&p.counter[1], 1u) == gridDim.x - 1 ? 1 : 0;
     }
     __syncthreads();
-    if (threadIdx.x == 0) atomicExch(&p.counter[1], 0u);
+    if (sm.task) {
+      init_counter_set(p, p.counter);
+      __syncthreads();
+      if (threadIdx.x == 0) atomicExch(&p.counter[1], 0u);
+    }
   }
 }
 

@@ -115,9 +115,14 @@ struct ZeroBlock {
   int32_t cols;
 };
 
-// Work counters of the FP64 kernel: three scalars, the status word at byte 128,
-// one counter per tail queue from byte 256.
-inline size_t counter_bytes(int nq) { return (size_t)(256 + 4 * nq + 255) / 256 * 256; }
+// Counter block of a plan: a 256-byte status block (the status word at byte
+// 128), then two sets of work counters used by alternate launches of the FP64
+// kernel (each launch prepares the other set for the next, so no launch has to
+// reset its own at exit; a launch captured into a graph resets its own set
+// instead).  A set: [0] next tile task, [1] CTAs finished (exit reset only),
+// [2] tail tasks taken, [64 + q] next task of tail queue q.
+inline size_t counter_set_bytes(int nq) { return (size_t)(256 + 4 * nq + 255) / 256 * 256; }
+inline size_t counter_bytes(int nq) { return 256 + 2 * counter_set_bytes(nq); }
 constexpr int kQueueCounterBase = 64;   // in uint32 units
 
 // Device status word values (first int of the status buffer).
@@ -145,8 +150,10 @@ struct Fp64Params {
   int32_t ntail;       // entries of the tail list (a multiple of kThreads, padding included)
   int32_t nct;         // tail tasks
   int32_t nq;          // queues (one per SM of the planned device)
-  uint32_t *counter;   // [0] next tile task, [1] CTAs finished, [2] tail tasks taken;
-                       // counter[64 + q]: next task of queue q.  All return to 0 at exit.
+  uint32_t *counter;       // this launch's counter set (zeroed by the previous launch or the host)
+  uint32_t *counter_next;  // the set the next launch uses: this launch zeroes it
+  int32_t reset_at_exit;   // 1 (counter_next null): the last CTA to finish returns this launch's set to
+                           // zero, for a launch captured into a graph that replays it
   int32_t *status;
   int64_t nA, nB, nC;  // elements of the buffers read and written (the checked instance tests them)
   int32_t check;       // 1: the checked instance

@@ -123,7 +123,7 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   auto up = [&](size_t o, const void *src, size_t n) -> bool {
     return n == 0 || cudaMemcpyAsync(b + o, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
   };
-  // work counters and status word must start at zero; the rest is overwritten
+  // status word and both counter sets start at zero; the rest of the array is overwritten
   if (cudaMemsetAsync(b, 0, n_ctr, s) != cudaSuccess) return BS_ERR_CUDA;
   if (!up(o_tasks, P->ts.tasks.data(), n_tasks) || !up(o_groups, P->gs.groups.data(), n_groups) ||
       !up(o_rsegs, P->gs.rsegs.data(), n_rsegs) || !up(o_ksegs, P->gs.ksegs.data(), n_ksegs) ||
@@ -165,7 +165,8 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
   p.ntail = (int32_t)ntail;
   p.nct = (int32_t)((ntail + kThreads - 1) / kThreads);
   fill_queue_params(&p, P->ts.tq_ptr, sm_map);
-  p.counter = (uint32_t *)b;
+  p.counter = (uint32_t *)(b + 256);
+  p.counter_next = (uint32_t *)(b + 256 + counter_set_bytes(nq));
   p.status = (int32_t *)(b + 128);
   const int64_t items = (int64_t)P->ts.tasks.size() + (ntail + kThreads - 1) / kThreads;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)sms * per_sm));

@@ -146,6 +146,7 @@ struct bs_plan {
   void *d_maps = nullptr;
   void *d_ws_a = nullptr, *d_ws_b = nullptr;
   uint32_t *d_counter = nullptr;
+  int counter_parity = 0;   // which counter set the next FP64 launch uses
   int32_t *d_status = nullptr;
   // phase events of bs_contract when profiling: before the gather, after it,
   // after the zero fill, after the grouped kernel

@@ -316,9 +316,15 @@ bs_status bs_plan_check_groups(const bs_plan *plan, int64_t *bad_group);
  * populated C element is overwritten; padding and absent blocks are not
  * touched.  A, B and C must not overlap.  Work: an optional gather, an optional
  * zero fill of C, one persistent grouped-GEMM kernel.  BF16 plans need A and B
- * 16-byte aligned (MISALIGNED otherwise).  A plan holds one workspace and one
- * work counter: do not run the same plan on two streams at once.  Errors found
- * on the device are reported by bs_plan_last_device_error. */
+ * 16-byte aligned (MISALIGNED otherwise).  A plan holds one workspace and two
+ * sets of work counters that alternate from call to call: do not run the same
+ * plan on two streams at once.  A call made while `stream` is being captured
+ * into a CUDA graph is recorded so that every replay of the graph gives the
+ * same result (its launch returns its counters to zero at exit); a BF16 plan
+ * must first have run once, outside the capture, with the same A and B
+ * pointers (a change of operand pointers re-encodes the tensor maps with a
+ * host synchronisation).  Errors found on the device are reported by
+ * bs_plan_last_device_error. */
 bs_status bs_contract(bs_plan *plan, const void *A, const void *B, void *C, void *stream);
 
 /* bs_contract with every access checked against the caller's buffer sizes
