@@ -1172,11 +1172,18 @@ bs_status bs_contract_host(bs_plan *P, const void *A_host, const void *B_host, v
   // A C buffer in pinned host memory that the device can address, under a plan
   // that writes every C element once (no zero fill, no accumulation): the
   // kernel stores C straight into it over the host link and no copy follows.
-  // That saves the copy's fixed cost; past a few MiB the copy engine moves C
-  // faster than the kernel's stores do, so larger C takes the copy.
+  // That pays when C is small (the copy's fixed cost is saved) or when the
+  // kernel spreads its C stores thinly over a long run (an FP64 contraction
+  // bound by its arithmetic, whose stores the link absorbs while the pipe
+  // works, so the copy after the kernel disappears).  A kernel that writes C
+  // faster than that (the BF16 path) runs slower storing over the link than
+  // the copy engine moves C afterwards, and takes the copy.
   constexpr size_t kDirectCBytes = (size_t)4 << 20;
+  constexpr double kDirectCBytesPerUs = 50e3;   // 50 GB/s of C over the modelled kernel time
+  const double model_us = P->stats.model_us > 0 ? P->stats.model_us : 0.0;
+  const bool thin_stores = model_us > 0 && (double)nc <= kDirectCBytesPerUs * model_us;
   void *c_direct = nullptr;
-  if (P->zero_blocks.empty() && nc <= kDirectCBytes) {
+  if (P->zero_blocks.empty() && (nc <= kDirectCBytes || thin_stores)) {
     cudaPointerAttributes at{};
     if (cudaPointerGetAttributes(&at, C_host) == cudaSuccess) {
       if (at.type == cudaMemoryTypeHost && at.devicePointer) c_direct = at.devicePointer;

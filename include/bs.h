@@ -349,9 +349,10 @@ bs_status bs_contract_checked(bs_plan *plan, const void *A, int64_t nA, const vo
  * device can address (cudaHostAlloc, cudaHostRegister), one copy kernel pulls
  * them in; otherwise each goes through the copy engine.  When C_host is pinned
  * host memory the device can address, the plan writes each C element once (no
- * zero fill) and C takes at most 4 MiB, the kernel stores C straight into
- * C_host: every populated element is written and the rest of C_host is left
- * unchanged.  Otherwise the whole C buffer is copied back and its padding and
+ * zero fill) and C is either at most 4 MiB or written at no more than 50 GB/s
+ * over the plan's modelled kernel time (stats.model_us), the kernel stores C
+ * straight into C_host: every populated element is written and the rest of
+ * C_host is left unchanged.  Otherwise the whole C buffer is copied back and its padding and
  * absent blocks arrive as zeros.  Pinned host memory gives the fastest calls. */
 bs_status bs_contract_host(bs_plan *plan, const void *A_host, const void *B_host, void *C_host,
                            void *stream);

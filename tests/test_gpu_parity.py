@@ -247,8 +247,9 @@ def test_host_buffer_entry_point_matches_device_entry_point(pol):
 
 
 def test_host_entry_point_large_pinned_c_is_copied_back():
-    """A pinned C larger than 4 MiB (workload 4: 55 MB of FP32) is not stored into
-    directly: it arrives by one copy of the whole buffer, padding as zeros."""
+    """A pinned C larger than 4 MiB that its kernel writes fast (workload 4: 55 MB
+    of FP32 in a few tens of microseconds) is not stored into directly: it
+    arrives by one copy of the whole buffer, padding as zeros."""
     r = Run(bsgen.config4())
     c_dev = r.run()
     pop = _populated(r)
@@ -259,6 +260,26 @@ def test_host_entry_point_large_pinned_c_is_copied_back():
     bs.contract_host(r.P, a_pin, b_pin, c_pin)
     got = c_pin.numpy()
     assert np.array_equal(got[pop], c_dev[pop]) and np.all(got[~pop] == 0)
+
+
+def test_host_entry_point_large_pinned_c_under_a_long_fp64_kernel_is_stored_directly():
+    """A pinned C far beyond 4 MiB whose FP64 kernel spreads its stores over
+    milliseconds (workload 3 on the contraction axis) is stored into directly:
+    every populated element matches the device entry point and the padding of
+    C_host keeps what it held."""
+    r = Run(bsgen.config3(), None, None, "blockrow|align16", **POLICIES["contraction"])
+    c_dev = r.run()
+    pop = _populated(r)
+    st = r.P.stats()
+    nc = r.P.c_layout.nelems * 8
+    assert (~pop).sum() > 0 and nc > (4 << 20) and nc <= 50e3 * st["model_us"]
+    a_pin = torch.from_numpy(r.a_host).pin_memory()
+    b_pin = torch.from_numpy(r.b_host).pin_memory()
+    c_pin = torch.full((r.P.c_layout.nelems,), float("nan"), dtype=torch.float64).pin_memory()
+    for _ in range(2):
+        bs.contract_host(r.P, a_pin, b_pin, c_pin)
+        got = c_pin.numpy()
+        assert np.array_equal(got[pop], c_dev[pop]) and np.all(np.isnan(got[~pop]))
 
 
 @pytest.mark.parametrize("seed", [71, 75, 78, 81])
