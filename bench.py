@@ -426,13 +426,20 @@ def bucket_record(bs, torch, flush, stream):
 
 
 def chain_record(bs, torch, flush, stream):
-    """Two chained contractions T = A B (free axis), Y = T D (contraction axis), T on the device."""
+    """Two chained contractions T = A B (free axis), Y = T D (contraction axis), T on the device;
+    then the same chain with each stage's axis chosen by the cost model."""
     w1, w2 = bsgen.chain2()
     A = bs.Layout(w1.rows, w1.inner, w1.rule_a, w1.layout_a, 8)
     B = bs.Layout(w1.inner, w1.cols, w1.rule_b, w1.layout_b, 8)
-    P1 = bs.Plan(A, B, bs.F64, axis_policy=bs.AXIS_FREE, c_layout_flags=w1.layout_c)
     D = bs.Layout(w2.inner, w2.cols, w2.rule_b, w2.layout_b, 8)
-    P2 = bs.Plan(P1.c_layout, D, bs.F64, axis_policy=bs.AXIS_CONTRACTION, c_layout_flags=w2.layout_c)
+    rec = _chain_run(bs, torch, flush, stream, w1, w2, A, B, D, bs.AXIS_FREE, bs.AXIS_CONTRACTION)
+    rec["auto"] = _chain_run(bs, torch, flush, stream, w1, w2, A, B, D, bs.AXIS_AUTO, bs.AXIS_AUTO)
+    return rec
+
+
+def _chain_run(bs, torch, flush, stream, w1, w2, A, B, D, axis1, axis2):
+    P1 = bs.Plan(A, B, bs.F64, axis_policy=axis1, c_layout_flags=w1.layout_c, **PLAN_OPTS)
+    P2 = bs.Plan(P1.c_layout, D, bs.F64, axis_policy=axis2, c_layout_flags=w2.layout_c, **PLAN_OPTS)
 
     def dev(w, op, L):
         b = L.blocks()
@@ -451,8 +458,9 @@ def chain_record(bs, torch, flush, stream):
     ms = statistics.median(time_steps(torch, step, 20, 3, flush, stream))
     s1, s2 = P1.stats(), P2.stats()
     fl = s1["useful_flops"] + s2["useful_flops"]
+    names = ["auto", "contraction", "free", "none"]
     return {"workload": "chain " + w1.name + " -> " + w2.name, "ms": ms, "gflops": fl / (ms * 1e-3) / 1e9,
-            "stage_axes": ["free", "contraction"], "launches": s1["launches"] + s2["launches"],
+            "stage_axes": [names[s1["axis"]], names[s2["axis"]]], "launches": s1["launches"] + s2["launches"],
             "useful_gflop": fl / 1e9, "triples": s1["triples"] + s2["triples"],
             "roofline_frac": fl / (ms * 1e-3) / 1e12 / (NOMINAL_SMS * FP64_FLOP_PER_CLK_PER_SM * NOMINAL_MAX_MHZ * 1e6 / 1e12)}
 
