@@ -701,6 +701,16 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
     if (P->pack_a) pack_list(P->A, P->A_pk, &P->pack_copies);
     P->pack_copies_a = (int32_t)P->pack_copies.size();
     if (P->pack_b) pack_list(P->B, P->B_pk, &P->pack_copies);
+    {
+      // every table the kernels index with 32 bits
+      const size_t lim = (size_t)(INT32_MAX - kThreads);
+      if (P->ts.tail_elems.size() / 2 > lim || P->ts.tasks.size() > lim || P->gs.groups.size() > lim ||
+          P->gs.rsegs.size() > lim || P->gs.ksegs.size() > lim || P->pack_copies.size() > lim ||
+          P->btasks.size() > lim || P->bstages.size() > lim) {
+        delete P;
+        return BS_ERR_OVERFLOW;
+      }
+    }
     bool any_atomic = false;
     for (const auto &g : P->gs.groups) any_atomic |= (g.flags & GF_ATOMIC) != 0;
     if (any_atomic) zero_list(P->C, cm, &P->zero_blocks);

@@ -75,6 +75,12 @@ bs_status build_layout(const AxisCopy &rows, const AxisCopy &cols, const Sparsit
                        int32_t elem_bytes, bs_layout *L) {
   if ((flags & ~15u) != 0 || (flags & 3u) == 3u) return BS_ERR_INVALID_ARG;
   if (elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8) return BS_ERR_INVALID_ARG;
+  // a group's M, N and K are sums of one axis's dimensions, held in 32 bits
+  for (const AxisCopy *ax : {&rows, &cols}) {
+    int64_t total = 0;
+    for (int32_t t = 0; t < ax->n; ++t) total += ax->d[t];
+    if (total > INT32_MAX) return BS_ERR_OVERFLOW;
+  }
   L->rows = rows;
   L->cols = cols;
   L->flags = flags;

@@ -108,7 +108,8 @@ typedef struct bs_block_info {
  * dimension) view into one buffer; "Interleaved vs contiguous": the
  * arrangement decides which blocks form one wider view).  elem_bytes (2, 4 or 8) matters only for ALIGN16.
  * Errors: INVALID_ARG (NULL, n < 0, dim < 1, z2 rule without parities, bad
- * flags or elem_bytes), OVERFLOW (element count beyond int64), OOM. */
+ * flags or elem_bytes), OVERFLOW (element count beyond int64, or an axis
+ * whose dimensions add up to more than INT32_MAX), OOM. */
 bs_status bs_layout_create(const bs_axis_desc *rows, const bs_axis_desc *cols, const bs_rule *rule,
                            uint32_t flags, int32_t elem_bytes, bs_layout **out);
 
@@ -227,7 +228,8 @@ typedef struct bs_plan_stats {
  * The plan copies what it needs: A and B layouts may be destroyed afterwards.
  * Device tables and workspaces are allocated here (cudaMalloc) on the current
  * device, unless opts->host_only.  Errors: INVALID_ARG, SHAPE_MISMATCH,
- * UNSUPPORTED, OOM, CUDA, OVERFLOW. */
+ * UNSUPPORTED, OOM, CUDA, OVERFLOW (a task, tail, segment or copy table longer
+ * than the kernels' 32-bit indices reach). */
 bs_status bs_plan_create(const bs_layout *A, const bs_layout *B, int32_t dtype,
                          const bs_plan_options *opts, bs_plan **out);
 

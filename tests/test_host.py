@@ -259,6 +259,22 @@ def test_errors_are_status_codes():
         bs.contract(P, 0, 0, 0)
 
 
+def test_axis_dimensions_beyond_32_bits_are_overflow():
+    """A group's M, N and K are sums of one axis's dimensions, held in 32 bits:
+    an axis adding up to more than INT32_MAX is refused at layout creation."""
+    small = bsgen.Axis([100], [1])
+    big = bsgen.Axis([0, 1], [2 ** 30, 2 ** 30])
+    with pytest.raises(bs.BsError) as e:
+        bs.Layout(big, small, bsgen.Rule(0, 0), "blockrow", 8)
+    assert e.value.code == 9 and bs.lib.bs_status_string(9) == b"size overflow"
+    with pytest.raises(bs.BsError) as e:
+        bs.Layout(small, big, bsgen.Rule(0, 0), "colpanel", 8)
+    assert e.value.code == 9
+    # one less fits (the rule populates no block, so nothing is allocated)
+    L = bs.Layout(bsgen.Axis([0, 1], [2 ** 30, 2 ** 30 - 1]), small, bsgen.Rule(0, 0), "blockrow", 8)
+    assert L.nelems == 0
+
+
 def test_empty_structure():
     """A rule that admits no block gives an empty plan and an empty C."""
     w = bsgen.config1()
