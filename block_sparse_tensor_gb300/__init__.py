@@ -24,7 +24,7 @@ AXIS_AUTO, AXIS_CONTRACTION, AXIS_FREE, AXIS_NONE = 0, 1, 2, 3
 DEBUG_WITHHOLD_COPY, DEBUG_MERGE_UNCHECKED = 1, 2
 ERR_HOLE = 10
 PACK_AUTO, PACK_NEVER, PACK_ALWAYS = 0, 1, 2
-LAYOUT_FLAGS = {"blockrow": 0, "rowpanel": 1, "colpanel": 2, "charge_sorted": 4, "align16": 8}
+LAYOUT_FLAGS = {"blockrow": 0, "rowpanel": 1, "colpanel": 2, "charge_sorted": 4, "align16": 8, "align64": 16}
 STATUS = {0: "ok", 1: "invalid argument", 2: "shape mismatch", 3: "unsupported", 4: "out of memory",
           5: "CUDA error", 6: "device wait timed out", 7: "misaligned", 8: "device check failed",
           9: "size overflow", 10: "group is not a hole-free view of its blocks"}

@@ -443,7 +443,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
   bs_plan_options_default(&o);
   if (opts) o = *opts;
   if (o.axis_policy < 0 || o.axis_policy > 3 || o.pack_policy < 0 || o.pack_policy > 2) return BS_ERR_INVALID_ARG;
-  if ((o.c_layout_flags & ~15u) || (o.c_layout_flags & 3u) == 3u) return BS_ERR_INVALID_ARG;
+  if ((o.c_layout_flags & ~31u) || (o.c_layout_flags & 3u) == 3u) return BS_ERR_INVALID_ARG;
   const int eb_in = dtype == BS_F64 ? 8 : 2;
   if (A->elem_bytes != eb_in || B->elem_bytes != eb_in) return BS_ERR_INVALID_ARG;
   if (!A->cols.same_as(B->rows)) return BS_ERR_SHAPE_MISMATCH;
@@ -554,7 +554,7 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
 
     const bool sorted_pack = true;
     auto packed = [&](const bs_layout &src, uint32_t mode, bs_layout *dst) {
-      uint32_t f = mode | (sorted_pack ? BS_LAYOUT_CHARGE_SORTED : 0) | (dtype == BS_BF16_F32 ? BS_LAYOUT_ALIGN16 : 0);
+      uint32_t f = mode | (sorted_pack ? BS_LAYOUT_CHARGE_SORTED : 0) | (dtype == BS_BF16_F32 ? BS_LAYOUT_ALIGN64 : 0);
       return build_layout(src.rows, src.cols, sparsity_of(src), f, src.elem_bytes, dst);
     };
 

@@ -14,10 +14,13 @@
 // first onto the least loaded CTA), unrolled into a flat list of 64-deep K
 // stages; the CTA preloads the head of both lists to shared memory, so the
 // copy and MMA threads never wait on a table in global memory.
-//   warp 0  TMA producer (one thread): per stage one A box 128 x 64 (K-major,
-//           128-byte swizzle) and up to four B boxes 64 x 64 (N-major, 128-byte
-//           swizzle).  It fills the first ring of stages straight from the
-//           global list while the rest of the CTA is still setting up;
+//   warp 0 and the last warp  TMA copies (one thread each, alternate stages:
+//           issuing a stage's copies costs a thread about the same time
+//           whatever their size, so two issuers keep the copy engine busier):
+//           per stage one A box 128 x 64 (K-major, 128-byte swizzle) and up
+//           to four B boxes 64 x 64 (N-major, 128-byte swizzle).  Thread 0
+//           fills the first ring of stages straight from the global list
+//           while the rest of the CTA is still setting up;
 //   warp 1  TMEM owner and MMA issuer (one thread): per stage up to four
 //           M128 x N=BN x K16 MMAs (one instruction block when all four reach
 //           real K) into 256-column FP32 slots used in rotation, so the
@@ -52,7 +55,9 @@ constexpr int kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kTmemCols = 512;                    // two 256-column FP32 accumulator slots
 constexpr int kEpiWarps = BS_BF16_EPI_WARPS;      // epilogue warps, a multiple of 4 (one group per TMEM lane quarter)
 static_assert(kEpiWarps % 4 == 0, "epilogue warps per lane quarter");
-constexpr int kThreadsBf16 = 64 + 32 * kEpiWarps;
+constexpr int kProducer1Warp = 2 + kEpiWarps;     // the second copy thread's warp, after the epilogue warps
+constexpr int kThreadsBf16 = 32 * (kProducer1Warp + 1);
+static_assert(kStages % 2 == 0, "each of the two copy threads owns every other stage");
 constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x 32 FP32 columns per epilogue warp
 constexpr int kTaskCache = 16;                    // head of this CTA's task list, in shared memory
 constexpr int kStageCache = 32;                   // head of this CTA's stage list, in shared memory
@@ -63,6 +68,7 @@ struct Ctl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint32_t issued[kStages];   // 1 + phase of the last copy issued into the stage, 0 if none
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -216,28 +222,56 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
   const char *maps = (const char *)p.maps;
   const Bf16Cta me = p.ctas[blockIdx.x];
 
-  // producer state (thread 0 only)
-  int ps = 0, pstage = 0;
-  uint32_t pphase = 0;
-  uint32_t outstanding = 0, issued_phase = 0;   // bit s: stage s has a copy in flight / its phase
-  auto issue = [&](const Bf16Stage &E) {
-    const uint32_t fb = smem_u32(&ctl->full[pstage]);
+  // Copy issue: stage ps of this CTA's list goes to ring slot ps % kStages.
+  // The slot's copies all complete on its full barrier; issued[] remembers
+  // the last phase so that a copy thread can wait out its copies on exit.
+  auto issue = [&](const Bf16Stage &E, int ps) {
+    const int slot = ps % kStages;
+    const uint32_t phase = (uint32_t)(ps / kStages) & 1u;
+    const uint32_t fb = smem_u32(&ctl->full[slot]);
     // test hook: CTA 0's first stage is never filled, so the MMA thread's
     // bounded wait on it runs out and the kernel reports a timeout
     const bool withhold = (p.debug_flags & 1) && blockIdx.x == 0 && ps == 0;
     if (!withhold) {
       mbar_expect_tx(fb, (uint32_t)(kATileBytes + E.nb * kBChunkBytes));
-      unsigned char *st = smem + (size_t)pstage * kStageBytes;
+      unsigned char *st = smem + (size_t)slot * kStageBytes;
       tma_load_2d(smem_u32(st), maps + (size_t)E.map_a * 128, fb, E.k0, E.m0);   // rows past the group read as zero
       const void *mb = maps + (size_t)E.map_b * 128;
       for (int c = 0; c < E.nb; ++c) tma_load_2d(smem_u32(st + kATileBytes + c * kBChunkBytes), mb, fb, E.n0 + 64 * c, E.k0);
-      outstanding |= 1u << pstage;
-      issued_phase = (issued_phase & ~(1u << pstage)) | (pphase << pstage);
+      ctl->issued[slot] = phase + 1u;
     }
-    if (++pstage == kStages) {
-      pstage = 0;
-      pphase ^= 1u;
+  };
+  // One copy thread's share after the first ring: stages first, first + 2, ...
+  // (slots of one parity), each once its slot is free.  Issuing a stage's
+  // copies takes its thread a fixed time whatever their size, so two threads
+  // issuing alternate stages keep the copy engine busier than one.
+  auto produce = [&](int first) {
+    // each stage's record is read one of this thread's stages ahead (past the
+    // shared-memory head of the list it comes from global memory)
+    Bf16Stage F = first < me.stage_count ? stage_at(p, scache, me, first) : Bf16Stage{};
+    for (int ps = first; ps < me.stage_count; ps += 2) {
+      const Bf16Stage E = F;
+      if (ps + 2 < me.stage_count) F = stage_at(p, scache, me, ps + 2);
+      const int slot = ps % kStages;
+      const uint32_t phase = (uint32_t)(ps / kStages) & 1u;
+      if (!mbar_wait(smem_u32(&ctl->empty[slot]), phase ^ 1u, abort_flag, p.timeout_ns)) {
+        record_timeout(p, ctl);
+        break;
+      }
+      issue(E, ps);
+      if (ps + 2 < me.stage_count) {   // warm the descriptor cache for this thread's next stage
+        prefetch_map(maps + (size_t)F.map_a * 128);
+        prefetch_map(maps + (size_t)F.map_b * 128);
+      }
     }
+    // Drain: every copy issued into this thread's slots completes before the
+    // CTA exits.  (On the normal path the MMA thread has consumed them all.)
+    for (int s = first % 2; s < kStages; s += 2)
+      if (ctl->issued[s]) {
+        const uint64_t t0 = gtime();
+        while (!mbar_try(smem_u32(&ctl->full[s]), ctl->issued[s] - 1u) && gtime() - t0 < p.timeout_ns) {
+        }
+      }
   };
 
   if (threadIdx.x == 0) {
@@ -250,12 +284,13 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       mbar_init(smem_u32(&ctl->tempty[a]), kEpiWarps);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
+    for (int s = 0; s < kStages; ++s) ctl->issued[s] = 0u;
     ctl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     // The first ring of stages needs no free slot: fill it from the global
     // list while the other warps allocate tensor memory and load the lists.
-    for (const int n = min(kStages, me.stage_count); ps < n; ++ps) issue(p.stages[me.stage_begin + ps]);
+    for (int ps = 0; ps < min(kStages, me.stage_count); ++ps) issue(p.stages[me.stage_begin + ps], ps);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&ctl->tmem_base)),
@@ -275,30 +310,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      for (; ps < me.stage_count; ++ps) {
-        const Bf16Stage E = stage_at(p, scache, me, ps);
-        if (!mbar_wait(smem_u32(&ctl->empty[pstage]), pphase ^ 1u, abort_flag, p.timeout_ns)) {
-          record_timeout(p, ctl);
-          break;
-        }
-        issue(E);
-        if (ps + 2 < me.stage_count) {   // warm the descriptor cache two stages ahead
-          const Bf16Stage F = stage_at(p, scache, me, ps + 2);
-          prefetch_map(maps + (size_t)F.map_a * 128);
-          prefetch_map(maps + (size_t)F.map_b * 128);
-        }
-      }
-      // Drain: every issued stage completes its transfer before the CTA exits.
-      // (On the normal path the MMA thread has consumed them all already.)
-      for (int s = 0; s < kStages; ++s)
-        if (outstanding >> s & 1u) {
-          uint64_t t0 = gtime();
-          while (!mbar_try(smem_u32(&ctl->full[s]), issued_phase >> s & 1u) && gtime() - t0 < p.timeout_ns) {
-          }
-        }
-    }
+    if (lane == 0) produce(kStages);   // ------------------------------ copies, even stages
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
@@ -310,8 +322,12 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       uint32_t phase = 0, te0 = 0, te1 = 0;   // ring phase; tempty phase per slot
       uint32_t d = tmem_base, idesc = 0, acc = 0;
       bool issued_any = false;
+      // each stage's record is read one stage ahead (past the shared-memory
+      // head of the list it comes from global memory)
+      Bf16Stage En = me.stage_count > 0 ? stage_at(p, scache, me, 0) : Bf16Stage{};
       for (int si = 0; si < me.stage_count; ++si) {
-        const Bf16Stage E = stage_at(p, scache, me, si);
+        const Bf16Stage E = En;
+        if (si + 1 < me.stage_count) En = stage_at(p, scache, me, si + 1);
         if (E.flags & kStageFirst) {
           if (!mbar_wait(smem_u32(&ctl->tempty[slot]), (slot ? te1 : te0) ^ 1u, abort_flag, p.timeout_ns)) {
             record_timeout(p, ctl);
@@ -356,6 +372,8 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
         }
       }
     }
+  } else if (warp == kProducer1Warp) {
+    if (lane == 0) produce(kStages + 1);   // -------------------------- copies, odd stages
   } else {
     // -------------------------------------------------------------- epilogue
     // A warp may read only TMEM lanes 32*(warp%4) .. +31 (tile rows).  Each

@@ -73,7 +73,7 @@ static inline int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * 
 
 bs_status build_layout(const AxisCopy &rows, const AxisCopy &cols, const Sparsity &sp, uint32_t flags,
                        int32_t elem_bytes, bs_layout *L) {
-  if ((flags & ~15u) != 0 || (flags & 3u) == 3u) return BS_ERR_INVALID_ARG;
+  if ((flags & ~31u) != 0 || (flags & 3u) == 3u) return BS_ERR_INVALID_ARG;
   if (elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8) return BS_ERR_INVALID_ARG;
   // a group's M, N and K are sums of one axis's dimensions, held in 32 bits
   for (const AxisCopy *ax : {&rows, &cols}) {
@@ -85,7 +85,7 @@ bs_status build_layout(const AxisCopy &rows, const AxisCopy &cols, const Sparsit
   L->cols = cols;
   L->flags = flags;
   L->elem_bytes = elem_bytes;
-  const int64_t al = (flags & BS_LAYOUT_ALIGN16) ? 16 / elem_bytes : 1;
+  const int64_t al = (flags & BS_LAYOUT_ALIGN64) ? 64 / elem_bytes : (flags & BS_LAYOUT_ALIGN16) ? 16 / elem_bytes : 1;
   const bool sorted = (flags & BS_LAYOUT_CHARGE_SORTED) != 0;
   const std::vector<int32_t> ro = sector_order(rows, sorted), co = sector_order(cols, sorted);
   std::vector<int32_t> col_rank(cols.n);

@@ -21,7 +21,7 @@ from . import build as _build
 
 _lib = None
 
-FLAG_BITS = {"blockrow": 0, "rowpanel": 1, "colpanel": 2, "charge_sorted": 4, "align16": 8}
+FLAG_BITS = {"blockrow": 0, "rowpanel": 1, "colpanel": 2, "charge_sorted": 4, "align16": 8, "align64": 16}
 
 
 def load(path: str):

@@ -38,6 +38,7 @@
 #define BSO_COLPANEL 2u
 #define BSO_CHARGE_SORTED 4u
 #define BSO_ALIGN16 8u
+#define BSO_ALIGN64 16u
 
 /* Allowed-charge rule: block (r, c) is populated iff
  * dq_min <= q_r - q_c <= dq_max and, when z2 is set, the parities are equal. */
@@ -90,7 +91,8 @@ static int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 /*
  * Offsets and leading dimensions of every populated block, as dense nr x nc
  * tables (off = -1 where the block is absent), in elements.  Rules:
- *   al = 16 / elem_bytes with ALIGN16, else 1;  w(c) = d_c rounded up to al.
+ *   al = 64 / elem_bytes with ALIGN64, else 16 / elem_bytes with ALIGN16,
+ *   else 1;  w(c) = d_c rounded up to al.
  *   blockrow : rows in order, then columns in order; each block is row-major
  *              with ld = w(c), placed right after the previous one.
  *   rowpanel : per row sector (in order) one row-major panel of d_r rows whose
@@ -102,7 +104,7 @@ static int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int32_t bso_layout(int32_t nr, const int32_t *rq, const uint8_t *rp, const int32_t *rd, int32_t nc,
                    const int32_t *cq, const uint8_t *cp, const int32_t *cd, const uint8_t *mask,
                    uint32_t flags, int32_t elem_bytes, int64_t *off, int64_t *ld, int64_t *nelems) {
-  int64_t al = (flags & BSO_ALIGN16) ? 16 / elem_bytes : 1;
+  int64_t al = (flags & BSO_ALIGN64) ? 64 / elem_bytes : (flags & BSO_ALIGN16) ? 16 / elem_bytes : 1;
   int sorted = (flags & BSO_CHARGE_SORTED) != 0;
   int32_t *ro = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nr > 0 ? nr : 1));
   int32_t *co = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nc > 0 ? nc : 1));

@@ -18,7 +18,7 @@ import oracle
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PKG = os.path.join(ROOT, "block_sparse_tensor_gb300")
 SRC = os.path.join(ROOT, "tests", "c_abi", "abi_check.c")
-FLAGS = {"blockrow": 0, "rowpanel": 1, "colpanel": 2, "charge_sorted": 4, "align16": 8}
+FLAGS = {"blockrow": 0, "rowpanel": 1, "colpanel": 2, "charge_sorted": 4, "align16": 8, "align64": 16}
 
 
 def _flags(name):

@@ -411,6 +411,29 @@ def test_full_size_every_block(cfg):
     compare_all(r, c)
 
 
+def test_config4_align64_layouts_every_block():
+    """The BF16 workload with every operand and C row on a 64-byte boundary."""
+    w = bsgen.config4()
+    r = Run(w, "rowpanel|charge_sorted|align64", "colpanel|charge_sorted|align64", "rowpanel|charge_sorted|align64")
+    assert r.P.stats()["packed_a"] == 0
+    compare_all(r, r.run())
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_align64_layouts_integer_inputs_bit_exact(seed):
+    """64-byte layouts on the FP64 paths (tail, tiles, gather) and the BF16 path."""
+    rng = np.random.default_rng(300 + seed)
+    w = _int_workload(seed, "bf16", rng.integers(130, 300, 3), rng.integers(20, 150, 4), rng.integers(30, 280, 3),
+                      f"int_bf16_a64_{seed}")
+    r = Run(w, "rowpanel|charge_sorted|align64", "colpanel|charge_sorted|align64", "rowpanel|align64")
+    compare(r, r.run(), exact=True)
+    wf = _int_workload(seed, "f64", rng.integers(1, 90, 4), rng.integers(1, 90, 4), rng.integers(1, 90, 4),
+                       f"int_f64_a64_{seed}")
+    for pol in ["contraction", "free", "contraction_pack"]:
+        rf = Run(wf, "blockrow|align64", "rowpanel|align64", "colpanel|align64", **POLICIES[pol])
+        compare(rf, rf.run(), exact=True)
+
+
 def test_config5_pack_path_every_block():
     w = bsgen.config5()
     r = Run(w, "blockrow", "blockrow", "blockrow", axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)

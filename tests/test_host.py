@@ -31,7 +31,8 @@ def test_library_exports_every_declared_symbol():
 
 
 LAYOUT_FLAGS = ["blockrow", "rowpanel", "colpanel", "blockrow|charge_sorted", "rowpanel|charge_sorted",
-                "colpanel|charge_sorted", "rowpanel|align16", "colpanel|charge_sorted|align16", "blockrow|align16"]
+                "colpanel|charge_sorted", "rowpanel|align16", "colpanel|charge_sorted|align16", "blockrow|align16",
+                "rowpanel|charge_sorted|align64", "colpanel|align64", "blockrow|align16|align64"]
 
 
 def lib_blocks_by_rc(layout):
