@@ -159,12 +159,14 @@ bs_status encode_maps(bs_plan *P, const void *A, const void *B) {
     const MapDesc &m = P->maps[t];
     const int eb = 2;
     const char *base = (const char *)(m.operand == 0 ? A : B) + m.off * eb;
-    cuuint64_t dims[2] = {(cuuint64_t)m.inner, (cuuint64_t)m.outer};
-    cuuint64_t strides[1] = {(cuuint64_t)(m.ld * eb)};
-    cuuint32_t box[2] = {(cuuint32_t)m.box_inner, (cuuint32_t)m.box_outer};
-    cuuint32_t es[2] = {1, 1};
+    const bool three = m.chunks > 0;
+    // 3-D: (64 columns of a chunk, rows, chunks 128 bytes apart)
+    cuuint64_t dims[3] = {(cuuint64_t)(three ? 64 : m.inner), (cuuint64_t)m.outer, (cuuint64_t)m.chunks};
+    cuuint64_t strides[2] = {(cuuint64_t)(m.ld * eb), (cuuint64_t)(64 * eb)};
+    cuuint32_t box[3] = {(cuuint32_t)m.box_inner, (cuuint32_t)m.box_outer, (cuuint32_t)m.box_chunks};
+    cuuint32_t es[3] = {1, 1, 1};
     CUtensorMap *out = (CUtensorMap *)(P->map_bytes.data() + t * sizeof(CUtensorMap));
-    CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)base, dims, strides, box, es,
+    CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, three ? 3 : 2, (void *)base, dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return BS_ERR_MISALIGNED;
@@ -176,12 +178,15 @@ bs_status encode_maps(bs_plan *P, const void *A, const void *B) {
 // pair per inner segment.
 void build_bf16(bs_plan *P) {
   const GroupSet &gs = P->gs;
-  std::map<std::tuple<int, int64_t, int64_t, int64_t, int64_t>, int32_t> seen;
-  auto map_id = [&](int op, int64_t off, int64_t inner, int64_t outer, int64_t ld, int bi, int bo) {
-    auto key = std::make_tuple(op, off, inner, outer, ld);
+  std::map<std::tuple<int, int64_t, int64_t, int64_t, int64_t, int, int>, int32_t> seen;
+  auto map_id = [&](int op, int64_t off, int64_t inner, int64_t outer, int64_t ld, int bi, int bo, int chunks = 0,
+                    int box_chunks = 0) {
+    auto key = std::make_tuple(op, off, inner, outer, ld, chunks, box_chunks);
     auto it = seen.find(key);
     if (it != seen.end()) return it->second;
     MapDesc m{op, off, inner, outer, ld, bi, bo};
+    m.chunks = chunks;
+    m.box_chunks = box_chunks;
     P->maps.push_back(m);
     int32_t id = (int32_t)P->maps.size() - 1;
     seen[key] = id;
@@ -196,6 +201,16 @@ void build_bf16(bs_plan *P) {
       Bf16Pair pr{};
       pr.map_a = map_id(0, k.ka, k.klen, g.m, k.kl, 64, 128);
       pr.map_b = map_id(1, k.kb, g.n, k.klen, k.ldb, 64, 64);
+      // a tile's whole 64-column chunks of B go in one 3-D box (one copy
+      // instruction instead of one per chunk); a ragged last chunk keeps its
+      // 2-D box, which stops at the view's edge
+      const int32_t whole = g.n / 64;
+      for (int c = 0; c <= 4; ++c) pr.map_b3[c] = -1;
+      for (int32_t n0 = 0; n0 < g.n; n0 += 256) {
+        const int32_t nfull = std::min<int32_t>(4, std::max<int32_t>(0, (g.n - n0) / 64));
+        if (nfull >= 2 && pr.map_b3[nfull] < 0)
+          pr.map_b3[nfull] = map_id(1, k.kb, 64 * (int64_t)whole, k.klen, k.ldb, 64, 64, whole, nfull);
+      }
       pr.klen = k.klen;
       P->bpairs.push_back(pr);
     }
@@ -257,6 +272,11 @@ void build_bf16(bs_plan *P) {
           e.m0 = T.m0;
           e.n0 = T.n0;
           e.nb = (int16_t)((T.bn + 63) / 64);
+          const int32_t nfull = std::min<int32_t>(e.nb, std::max<int32_t>(0, (T.n - T.n0) / 64));
+          if (nfull >= 2 && pr.map_b3[nfull] >= 0) {
+            e.map_b3 = pr.map_b3[nfull];
+            e.flags = (int16_t)(nfull << 8);
+          }
           e.ksteps = (int16_t)std::min(4, (pr.klen - k0 + 15) / 16);
           e.bn = (int16_t)T.bn;
           P->bstages.push_back(e);

@@ -128,6 +128,13 @@ __device__ __forceinline__ void prefetch_map(const void *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint32_t mbar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(map), "r"(mbar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint32_t mbar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
@@ -236,8 +243,11 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       mbar_expect_tx(fb, (uint32_t)(kATileBytes + E.nb * kBChunkBytes));
       unsigned char *st = smem + (size_t)slot * kStageBytes;
       tma_load_2d(smem_u32(st), maps + (size_t)E.map_a * 128, fb, E.k0, E.m0);   // rows past the group read as zero
+      // the tile's first nb3 whole B chunks in one 3-D box, the rest chunk by chunk
+      const int nb3 = E.flags >> 8;
+      if (nb3 > 0) tma_load_3d(smem_u32(st + kATileBytes), maps + (size_t)E.map_b3 * 128, fb, 0, E.k0, E.n0 >> 6);
       const void *mb = maps + (size_t)E.map_b * 128;
-      for (int c = 0; c < E.nb; ++c) tma_load_2d(smem_u32(st + kATileBytes + c * kBChunkBytes), mb, fb, E.n0 + 64 * c, E.k0);
+      for (int c = nb3; c < E.nb; ++c) tma_load_2d(smem_u32(st + kATileBytes + c * kBChunkBytes), mb, fb, E.n0 + 64 * c, E.k0);
       ctl->issued[slot] = phase + 1u;
     }
   };
@@ -261,7 +271,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) bf16_grouped_kernel(const Bf1
       issue(E, ps);
       if (ps + 2 < me.stage_count) {   // warm the descriptor cache for this thread's next stage
         prefetch_map(maps + (size_t)F.map_a * 128);
-        prefetch_map(maps + (size_t)F.map_b * 128);
+        prefetch_map(maps + (size_t)((F.flags >> 8) ? F.map_b3 : F.map_b) * 128);
       }
     }
     // Drain: every copy issued into this thread's slots completes before the

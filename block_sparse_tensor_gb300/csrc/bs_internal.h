@@ -181,7 +181,7 @@ struct Bf16Pair {
   int32_t map_a;   // index of the A tensor map (rows of the group x d_k)
   int32_t map_b;   // index of the B tensor map (d_k x cols of the group)
   int32_t klen;    // d_k
-  int32_t pad_;
+  int32_t map_b3[5];   // 3-D B map whose box takes c whole 64-column chunks at once (c = 2..4), -1 if none
 };
 
 struct Bf16Task {
@@ -210,8 +210,8 @@ struct Bf16Stage {
   int16_t nb;       // B boxes (64 columns each)
   int16_t ksteps;   // K16 MMA steps that reach real K (1..4)
   int16_t bn;       // UMMA N of the tile
-  int16_t flags;    // kStageFirst | kStageLast
-  int32_t pad_;
+  int16_t flags;    // kStageFirst | kStageLast; bits 8-15: B chunks copied by map_b3 (0: none)
+  int32_t map_b3;   // 3-D B map taking the tile's first (flags >> 8) chunks in one box
 };
 static_assert(sizeof(Bf16Stage) == 32, "stage record");
 

@@ -96,6 +96,12 @@ struct MapDesc {
   int64_t ld;           // elements between rows
   int32_t box_inner;
   int32_t box_outer;
+  // 0: a 2-D map of the view (inner x outer).  Otherwise a 3-D map of its first
+  // `chunks` whole 64-column chunks (64 x outer x chunks, the chunk stride 128
+  // bytes), whose box takes box_chunks chunks at once; the view's footprint
+  // (inner = 64 * chunks) stays inside the 2-D view's.
+  int32_t chunks = 0;
+  int32_t box_chunks = 0;
 };
 
 }  // namespace bs
