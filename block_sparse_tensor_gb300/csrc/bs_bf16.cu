@@ -12,15 +12,16 @@
 //
 // One CTA per SM.  At plan time each CTA gets its own task list (longest
 // first onto the least loaded CTA), unrolled into a flat list of 64-deep K
-// stages; the CTA preloads the head of both lists to shared memory, so the
-// copy and MMA threads never wait on a table in global memory.
+// stages; the CTA preloads the head of both lists to shared memory and reads
+// the rest one stage ahead of its use.
 //   warp 0 and the last warp  TMA copies (one thread each, alternate stages:
 //           issuing a stage's copies costs a thread about the same time
 //           whatever their size, so two issuers keep the copy engine busier):
-//           per stage one A box 128 x 64 (K-major, 128-byte swizzle) and up
-//           to four B boxes 64 x 64 (N-major, 128-byte swizzle).  Thread 0
-//           fills the first ring of stages straight from the global list
-//           while the rest of the CTA is still setting up;
+//           per stage one A box 128 x 64 (K-major, 128-byte swizzle) and the
+//           tile's B columns, 64 x 64 chunks (N-major, 128-byte swizzle), its
+//           whole chunks in one 3-D box and a ragged last chunk in a 2-D box.
+//           Thread 0 fills the first ring of stages straight from the global
+//           list while the rest of the CTA is still setting up;
 //   warp 1  TMEM owner and MMA issuer (one thread): per stage up to four
 //           M128 x N=BN x K16 MMAs (one instruction block when all four reach
 //           real K) into 256-column FP32 slots used in rotation, so the
