@@ -85,7 +85,8 @@ typedef struct bs_rule {
  * ALIGN64 rounds it up to a multiple of 64 bytes instead (and wins over
  * ALIGN16): every row of every block then starts on a 64-byte boundary, which
  * the BF16 kernel's tensor-map copies move markedly faster than rows that
- * start 16 bytes off one. */
+ * start 16 bytes off one.  (FP64 plans do not gain from it: the padding
+ * between narrow blocks splits a group's K into more views.) */
 enum {
   BS_LAYOUT_BLOCKROW = 0,
   BS_LAYOUT_ROWPANEL = 1,
