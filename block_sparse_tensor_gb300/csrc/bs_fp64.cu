@@ -295,11 +295,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Pa
   // Then the tail: CTA-sized tasks (kThreads consecutive outputs of the tail
   // list, so the 8 warps walk the same B rows through L1), dealt at plan time
   // longest first onto one queue per SM, each queue's tasks numbered
-  // consecutively.  A CTA serves the queue of the SM it runs on, claiming the
-  // queue's next task while it still runs the current one; once that queue is
-  // empty it takes tasks from the others (so no output depends on every SM
-  // receiving CTAs).  Thread 0 claims; the CTA runs the task, warp w on its
-  // w-th 32 outputs.
+  // consecutively.  A CTA serves the queue of the SM it runs on; once that
+  // queue is empty it takes tasks from the others (so no output depends on
+  // every SM receiving CTAs).  Thread 0 claims; the CTA runs the task, warp w
+  // on its w-th 32 outputs.
   if (p.nct > 0) {
     const int warp = threadIdx.x >> 5;
     int q0 = 0, qk = 0;          // thread 0: home queue, queues emptied so far
