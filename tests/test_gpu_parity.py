@@ -411,6 +411,19 @@ def test_full_size_every_block(cfg):
     compare_all(r, c)
 
 
+@pytest.mark.parametrize("n", [16, 64, 100, 128, 200, 256, 320, 384, 515])
+@pytest.mark.parametrize("align", ["align16", "align64"])
+def test_bf16_column_widths_integer_inputs_bit_exact(n, align):
+    """Column sectors of width n: whole 64-column chunks of a tile come in one 3-D box
+    (2 to 4 of them), a ragged last chunk in its own 2-D box; tiles past the first
+    256 columns take fewer whole chunks."""
+    rng = np.random.default_rng(400 + n)
+    w = _int_workload(n, "bf16", rng.integers(100, 300, 2), rng.integers(40, 140, 3), [n, n, n // 2 + 8],
+                      f"int_bf16_n{n}_{align}")
+    r = Run(w, f"rowpanel|charge_sorted|{align}", f"colpanel|charge_sorted|{align}", f"rowpanel|{align}")
+    compare(r, r.run(), exact=True)
+
+
 def test_config4_align64_layouts_every_block():
     """The BF16 workload with every operand and C row on a 64-byte boundary."""
     w = bsgen.config4()
