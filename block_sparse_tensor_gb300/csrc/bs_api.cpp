@@ -178,10 +178,11 @@ bs_status encode_maps(bs_plan *P, const void *A, const void *B) {
 // pair per inner segment.
 void build_bf16(bs_plan *P) {
   const GroupSet &gs = P->gs;
-  std::map<std::tuple<int, int64_t, int64_t, int64_t, int64_t, int, int>, int32_t> seen;
+  std::map<std::tuple<int, int64_t, int64_t, int64_t, int64_t, int, int, int, int>, int32_t> seen;
   auto map_id = [&](int op, int64_t off, int64_t inner, int64_t outer, int64_t ld, int bi, int bo, int chunks = 0,
                     int box_chunks = 0) {
-    auto key = std::make_tuple(op, off, inner, outer, ld, chunks, box_chunks);
+    // the box is part of a map: the same view with another box is another map
+    auto key = std::make_tuple(op, off, inner, outer, ld, bi, bo, chunks, box_chunks);
     auto it = seen.find(key);
     if (it != seen.end()) return it->second;
     MapDesc m{op, off, inner, outer, ld, bi, bo};
