@@ -1184,7 +1184,7 @@ bs_status bs_plan_profile(bs_plan *P, bs_phase_times *out) {
   out->gather_ms = P->pack_copies.empty() ? 0.0 : t[0];
   out->zero_ms = P->zero_blocks.empty() ? 0.0 : t[1];
   out->kernel_ms = t[2];
-  out->total_ms = (double)t[0] + t[1] + t[2];
+  out->total_ms = out->gather_ms + out->zero_ms + out->kernel_ms;
   out->gather_bytes = 2 * P->stats.packed_bytes;
   return BS_OK;
 }

@@ -54,3 +54,34 @@ def test_non_empty_operands_with_empty_product(dtype):
     A, B = _contract_empty(_axis([0, 1, 2, 3], 8), _axis([0, 1, 2, 3], 8), _axis([0], 8),
                            bsgen.Rule(3, 3), bsgen.Rule(2, 3), dtype)
     assert A.nelems > 0 and B.nelems > 0
+
+
+@pytest.mark.parametrize("case", ["gather", "zero_fill", "plain"])
+def test_phase_profile_reports_each_phase(case):
+    """A plan built with profile=1 reports the gather, zero fill and kernel
+    times of its last contraction (0 for a phase it does not have), their sum,
+    and the gather's bytes; a plan without profiling refuses."""
+    w = bsgen.config2()
+    lay = {"gather": ("blockrow", "blockrow", "blockrow"), "zero_fill": (None, None, None),
+           "plain": (None, None, None)}[case]
+    opts = {"gather": dict(axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS),
+            "zero_fill": dict(axis_policy=bs.AXIS_FREE), "plain": dict(axis_policy=bs.AXIS_CONTRACTION)}[case]
+    A = bs.Layout(w.rows, w.inner, w.rule_a, lay[0] or w.layout_a, 8)
+    B = bs.Layout(w.inner, w.cols, w.rule_b, lay[1] or w.layout_b, 8)
+    P = bs.Plan(A, B, bs.F64, c_layout_flags=lay[2] or w.layout_c, profile=1, **opts)
+    a = torch.randn(A.nelems, dtype=torch.float64, device="cuda")
+    b = torch.randn(B.nelems, dtype=torch.float64, device="cuda")
+    c = torch.zeros(P.c_layout.nelems, dtype=torch.float64, device="cuda")
+    with pytest.raises(bs.BsError):
+        P.profile()   # not run yet
+    bs.contract(P, a, b, c)
+    t = P.profile()
+    st = P.stats()
+    assert t["kernel_ms"] > 0
+    assert (t["gather_ms"] > 0) == (case == "gather") and (t["zero_ms"] > 0) == (case == "zero_fill")
+    assert t["gather_bytes"] == (2 * st["packed_bytes"] if case == "gather" else 0)
+    assert abs(t["total_ms"] - (t["gather_ms"] + t["zero_ms"] + t["kernel_ms"])) < 1e-6
+    Q = bs.Plan(A, B, bs.F64, c_layout_flags=lay[2] or w.layout_c, **opts)
+    bs.contract(Q, a, b, c)
+    with pytest.raises(bs.BsError):
+        Q.profile()   # built without profiling
