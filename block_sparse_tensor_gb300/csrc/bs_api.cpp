@@ -1075,6 +1075,14 @@ static bs_status contract_impl(bs_plan *P, const void *A, const void *B, void *C
       for (const auto &t : P->btasks)
         if (!view_inside(t.c_off, t.m, t.n, t.ldc, sizes[2])) return BS_ERR_DEVICE;
   }
+  if (P->dtype == BS_BF16_F32 && !P->btasks.empty() && (P->maps_a_ptr != Ause || P->maps_b_ptr != Buse)) {
+    // New operand pointers: the tensor maps are re-encoded, uploaded and
+    // waited for, which a stream being captured into a graph cannot do;
+    // refuse before anything is enqueued, so that the capture stays valid.
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    BS_CUDA(cudaStreamIsCapturing(s, &capturing));
+    if (capturing != cudaStreamCaptureStatusNone) return BS_ERR_UNSUPPORTED;
+  }
   const bool prof = P->opts.profile != 0;
   if (prof) {
     for (auto &e : P->ev)

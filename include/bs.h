@@ -331,7 +331,8 @@ bs_status bs_plan_check_groups(const bs_plan *plan, int64_t *bad_group);
  * same result (its launch returns its counters to zero at exit); a BF16 plan
  * must first have run once, outside the capture, with the same A and B
  * pointers (a change of operand pointers re-encodes the tensor maps with a
- * host synchronisation).  Errors found on the device are reported by
+ * host synchronisation, so inside a capture such a call returns UNSUPPORTED
+ * before it enqueues anything and the capture stays valid).  Errors found on the device are reported by
  * bs_plan_last_device_error. */
 bs_status bs_contract(bs_plan *plan, const void *A, const void *B, void *C, void *stream);
 

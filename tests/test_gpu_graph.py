@@ -86,3 +86,26 @@ def test_eager_calls_then_graph_replays_repeat_the_first_result(name, make, lay,
         torch.cuda.synchronize()
         assert bs.last_device_error(P) == 0
         assert _same(c, ref)
+
+
+def test_bf16_capture_with_new_operand_pointers_is_refused_and_capture_survives():
+    """A BF16 call with operand pointers its tensor maps were not encoded for must
+    upload new maps and wait for them, which a capture cannot hold: the call
+    returns UNSUPPORTED (3) before it enqueues anything, the capture ends
+    cleanly, and the same call made eagerly afterwards gives the first result."""
+    P, a, b, c = _setup(bsgen.config4())
+    bs.contract(P, a, b, c, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert bs.last_device_error(P) == 0
+    ref = c.clone()
+    a2, b2 = a.clone(), b.clone()
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(bs.BsError) as err:
+        with torch.cuda.graph(g):
+            bs.contract(P, a2, b2, c, stream=torch.cuda.current_stream())
+    assert err.value.code == 3
+    c.zero_()
+    bs.contract(P, a2, b2, c, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert bs.last_device_error(P) == 0
+    assert torch.equal(c, ref)
