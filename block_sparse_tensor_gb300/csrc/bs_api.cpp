@@ -1200,6 +1200,12 @@ bs_status bs_plan_profile(bs_plan *P, bs_phase_times *out) {
 bs_status bs_contract_host(bs_plan *P, const void *A_host, const void *B_host, void *C_host, void *stream) {
   if (!P || !A_host || !B_host || !C_host || P->opts.host_only) return BS_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
+  {
+    // the call waits for its own copies: not something a graph capture can hold
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    BS_CUDA(cudaStreamIsCapturing(s, &capturing));
+    if (capturing != cudaStreamCaptureStatusNone) return BS_ERR_UNSUPPORTED;
+  }
   const size_t eb = P->dtype == BS_F64 ? 8 : 2, ec = P->dtype == BS_F64 ? 8 : 4;
   const size_t na = (size_t)P->A.nelems * eb, nb = (size_t)P->B.nelems * eb, nc = (size_t)P->C.nelems * ec;
   if (!P->d_host_c) {

@@ -362,7 +362,9 @@ bs_status bs_contract_checked(bs_plan *plan, const void *A, int64_t nA, const vo
  * over the plan's modelled kernel time (stats.model_us), the kernel stores C
  * straight into C_host: every populated element is written and the rest of
  * C_host is left unchanged.  Otherwise the whole C buffer is copied back and its padding and
- * absent blocks arrive as zeros.  Pinned host memory gives the fastest calls. */
+ * absent blocks arrive as zeros.  Pinned host memory gives the fastest calls.
+ * On a stream that is being captured into a graph the call returns
+ * UNSUPPORTED before it enqueues anything (it has to wait for its copies). */
 bs_status bs_contract_host(bs_plan *plan, const void *A_host, const void *B_host, void *C_host,
                            void *stream);
 

@@ -109,3 +109,23 @@ def test_bf16_capture_with_new_operand_pointers_is_refused_and_capture_survives(
     torch.cuda.synchronize()
     assert bs.last_device_error(P) == 0
     assert torch.equal(c, ref)
+
+
+def test_host_buffer_call_inside_a_capture_is_refused():
+    """bs_contract_host synchronizes its stream, which a capture cannot hold: inside
+    one it returns UNSUPPORTED (3) before it enqueues anything and the capture ends
+    cleanly; outside, the same call gives the device call's result."""
+    w = bsgen.config1()
+    P, a, b, c = _setup(w)
+    bs.contract(P, a, b, c, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ref = c.cpu().numpy()
+    ah, bh = a.cpu().numpy(), b.cpu().numpy()
+    ch = np.zeros(c.numel(), ref.dtype)
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(bs.BsError) as err:
+        with torch.cuda.graph(g):
+            bs.contract_host(P, ah, bh, ch, stream=torch.cuda.current_stream())
+    assert err.value.code == 3
+    bs.contract_host(P, ah, bh, ch)
+    assert _same(torch.from_numpy(ch), torch.from_numpy(ref))
