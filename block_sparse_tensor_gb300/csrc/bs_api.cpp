@@ -88,12 +88,12 @@ int64_t populated_elems(const bs_layout &L) {
   return s;
 }
 
-// Block copies of the gather (one warp each), split into row bands of at most
-// 2048 elements so one huge block does not serialise the launch on a few
-// warps, and listed largest first so the warps that take them in turn get
-// equal shares.
-void pack_list(const bs_layout &src, const bs_layout &dst, std::vector<PackCopy> *out) {
-  const size_t first = out->size();
+// Block copies of the gather, split into row bands of at most 2048 elements
+// so one huge block does not serialise the launch on a few warps, and listed
+// largest first so the warps that take them in turn get equal shares.  Copies
+// of at most kPackSmallElems elements go to `small` (moved four to a warp).
+void pack_list(const bs_layout &src, const bs_layout &dst, std::vector<PackCopy> *big, std::vector<PackCopy> *small) {
+  std::vector<PackCopy> all;
   for (const auto &b : src.blocks) {
     const auto &d = dst.blocks[dst.find(b.row, b.col)];
     const int32_t band = std::max<int32_t>(1, 2048 / b.cols);
@@ -105,12 +105,13 @@ void pack_list(const bs_layout &src, const bs_layout &dst, std::vector<PackCopy>
       c.dst_ld = d.ld;
       c.rows = std::min(band, b.rows - r0);
       c.cols = b.cols;
-      out->push_back(c);
+      all.push_back(c);
     }
   }
-  std::stable_sort(out->begin() + first, out->end(), [](const PackCopy &x, const PackCopy &y) {
+  std::stable_sort(all.begin(), all.end(), [](const PackCopy &x, const PackCopy &y) {
     return (int64_t)x.rows * x.cols > (int64_t)y.rows * y.cols;
   });
+  for (const auto &c : all) ((int64_t)c.rows * c.cols <= kPackSmallElems ? small : big)->push_back(c);
 }
 
 void zero_list(const bs_layout &C, const std::vector<uint8_t> *cmask, std::vector<ZeroBlock> *out) {
@@ -719,9 +720,18 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
       P->axis = BS_AXIS_CONTRACTION;
       build_bf16(P);
     }
-    if (P->pack_a) pack_list(P->A, P->A_pk, &P->pack_copies);
-    P->pack_copies_a = (int32_t)P->pack_copies.size();
-    if (P->pack_b) pack_list(P->B, P->B_pk, &P->pack_copies);
+    {
+      std::vector<PackCopy> big_a, small_a, big_b, small_b;
+      if (P->pack_a) pack_list(P->A, P->A_pk, &big_a, &small_a);
+      if (P->pack_b) pack_list(P->B, P->B_pk, &big_b, &small_b);
+      auto &pc = P->pack_copies;
+      pc.clear();
+      for (const auto *v : {&big_a, &big_b, &small_a, &small_b}) pc.insert(pc.end(), v->begin(), v->end());
+      P->pack_split.big_a = (int32_t)std::min<size_t>(big_a.size(), INT32_MAX);
+      P->pack_split.big = (int32_t)std::min<size_t>(big_a.size() + big_b.size(), INT32_MAX);
+      P->pack_split.small_a = (int32_t)std::min<size_t>(big_a.size() + big_b.size() + small_a.size(), INT32_MAX);
+      P->pack_split.total = (int32_t)std::min<size_t>(pc.size(), INT32_MAX);
+    }
     {
       // every table the kernels index with 32 bits
       const size_t lim = (size_t)(INT32_MAX - kThreads);
@@ -1062,7 +1072,7 @@ static bs_status contract_impl(bs_plan *P, const void *A, const void *B, void *C
     // the zero fill's writes and the BF16 tensor maps' views
     for (size_t t = 0; t < P->pack_copies.size(); ++t) {
       const PackCopy &c = P->pack_copies[t];
-      const bool of_a = (int32_t)t < P->pack_copies_a;
+      const bool of_a = P->pack_split.of_a((int64_t)t);
       if (!view_inside(c.src, c.rows, c.cols, c.src_ld, sizes[of_a ? 0 : 1])) return BS_ERR_DEVICE;
     }
     for (const auto &z : P->zero_blocks)
@@ -1094,13 +1104,13 @@ static bs_status contract_impl(bs_plan *P, const void *A, const void *B, void *C
     pp.src = A;
     pp.dst = P->d_ws_a;
     pp.copies = P->d_pack;
-    pp.ncopies = P->pack_copies_a;
+    pp.ncopies = P->pack_split.total;
     pp.elem_bytes = P->dtype == BS_F64 ? 8 : 2;
     // one launch gathers both operands: copies [0, n_a) read A, the rest read B
     PackParams pb = pp;
     pb.src = B;
     pb.dst = P->d_ws_b;
-    BS_CUDA(launch_pack2(pp, pb, (int32_t)P->pack_copies.size(), P->sm_count, s));
+    BS_CUDA(launch_pack2(pp, pb, P->pack_split, P->sm_count, s));
   }
   if (prof) BS_CUDA(cudaEventRecord(P->ev[1], s));
   if (!P->zero_blocks.empty())

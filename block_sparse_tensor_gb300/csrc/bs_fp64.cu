@@ -369,19 +369,21 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Pa
 
 // The gather: one warp per block copy, copies listed largest first at plan
 // time and dealt to the warps in turn (each warp fetches its next copy's
-// descriptor while it moves the current one).  A copy is moved in 16-byte
-// units when both views allow it (every row start 16-byte aligned and whole
-// rows of units), else element by element.  The warp walks the copy's
-// (row, column) positions 32 at a time with four loads in flight per lane and
-// divides no index: rows of at most 32 units map each lane to one fixed
-// (row offset, column) pair, so a step covers floor(32 / cols) rows; wider
-// rows advance each lane's position by 32 columns, wrapping to the next row.
-template <class U>
+// descriptor while it moves the current one); then the small copies (at most
+// kPackSmallElems elements), four to a warp, 8 lanes each, so that a warp has
+// four of them in flight instead of waiting on each in turn.  A copy is moved
+// in 16-byte units when both views allow it (every row start 16-byte aligned
+// and whole rows of units), else element by element.  A group of G lanes
+// walks the copy's (row, column) positions G at a time with four loads in
+// flight per lane and divides no index: rows of at most G units map each lane
+// to one fixed (row offset, column) pair, so a step covers floor(G / cols)
+// rows; wider rows advance each lane's position by G columns, wrapping to the
+// next row.
+template <class U, int G, int kU>
 __device__ __forceinline__ void copy_2d(const U *__restrict__ src, int64_t sld, U *__restrict__ dst, int64_t dld,
                                         int rows, int cols, int lane) {
-  constexpr int kU = 4;
-  if (cols <= 32) {
-    const int rpw = 32 / cols;
+  if (cols <= G) {
+    const int rpw = G / cols;
     const int lr = lane / cols, lc = lane - lr * cols;
     if (lr >= rpw) return;
     const U *sp = src + lc;
@@ -397,7 +399,7 @@ __device__ __forceinline__ void copy_2d(const U *__restrict__ src, int64_t sld, 
     for (; r < rows; r += rpw) dp[(int64_t)r * dld] = __ldg(sp + (int64_t)r * sld);
     return;
   }
-  // cols > 32: a step of 32 positions moves a lane at most into the next row
+  // cols > G: a step of G positions moves a lane at most into the next row
   int r = 0, c = lane;
   for (;;) {
     int rr[kU], cc[kU];
@@ -405,7 +407,7 @@ __device__ __forceinline__ void copy_2d(const U *__restrict__ src, int64_t sld, 
     for (int q = 0; q < kU; ++q) {
       rr[q] = r;
       cc[q] = c;
-      c += 32;
+      c += G;
       if (c >= cols) {
         c -= cols;
         ++r;
@@ -422,32 +424,54 @@ __device__ __forceinline__ void copy_2d(const U *__restrict__ src, int64_t sld, 
   }
 }
 
-template <class T>
-__global__ void pack_kernel(PackParams a, PackParams b, int32_t ntotal) {
+// One copy by a group of G lanes (lane = the lane's index inside the group),
+// kU loads in flight per lane.
+template <class T, int G, int kU>
+__device__ __forceinline__ void pack_one(const PackParams &pp, const PackCopy &cur, int lane) {
   constexpr int V = 16 / (int)sizeof(T);
+  const T *src = (const T *)pp.src + cur.src;
+  T *dst = (T *)pp.dst + cur.dst;
+  const bool base16 = (((uintptr_t)pp.src | (uintptr_t)pp.dst) & 15u) == 0;
+  int64_t sld = cur.src_ld, dld = cur.dst_ld;
+  int rows = cur.rows, cols = cur.cols;
+  if (sld == cols && dld == cols) {   // contiguous on both sides: one flat row
+    cols = rows * cols;
+    rows = 1;
+    sld = dld = cols;
+  }
+  if (base16 && ((cur.src | cur.dst | sld | dld | (int64_t)cols) % V) == 0)
+    copy_2d<int4, G, kU>((const int4 *)src, sld / V, (int4 *)dst, dld / V, rows, cols / V, lane);
+  else
+    copy_2d<T, G, kU>(src, sld, dst, dld, rows, cols, lane);
+}
+
+constexpr int kPackGroup = 8, kPackGroupU = 4;   // lanes per small copy, loads in flight per lane
+
+template <class T>
+__global__ void __launch_bounds__(256, 4) pack_kernel(PackParams a, PackParams b, PackSplit sp) {
   const int lane = threadIdx.x & 31;
+  const int gw = (int)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
   const int nw = (int)(gridDim.x * (blockDim.x >> 5));
-  int c = (int)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
   PackCopy cp;
-  if (c < ntotal) cp = a.copies[c];
-  for (; c < ntotal; c += nw) {
+  // whole-warp copies
+  int c = gw;
+  if (c < sp.big) cp = a.copies[c];
+  for (; c < sp.big; c += nw) {
     const PackCopy cur = cp;
-    if (c + nw < ntotal) cp = a.copies[c + nw];   // the next descriptor, in flight meanwhile
-    const PackParams &pp = c < a.ncopies ? a : b;
-    const T *src = (const T *)pp.src + cur.src;
-    T *dst = (T *)pp.dst + cur.dst;
-    const bool base16 = (((uintptr_t)pp.src | (uintptr_t)pp.dst) & 15u) == 0;
-    int64_t sld = cur.src_ld, dld = cur.dst_ld;
-    int rows = cur.rows, cols = cur.cols;
-    if (sld == cols && dld == cols) {   // contiguous on both sides: one flat row
-      cols = rows * cols;
-      rows = 1;
-      sld = dld = cols;
-    }
-    if (base16 && ((cur.src | cur.dst | sld | dld | (int64_t)cols) % V) == 0)
-      copy_2d<int4>((const int4 *)src, sld / V, (int4 *)dst, dld / V, rows, cols / V, lane);
-    else
-      copy_2d<T>(src, sld, dst, dld, rows, cols, lane);
+    if (c + nw < sp.big) cp = a.copies[c + nw];   // the next descriptor, in flight meanwhile
+    pack_one<T, 32, 4>(c < sp.big_a ? a : b, cur, lane);
+  }
+  // small copies, dealt from the last warp backwards (so that when there are
+  // warps to spare, a warp takes whole-warp copies or small ones, not both):
+  // lane group g of warp nw-1-r takes copies big + kPerWarp r + g, then every
+  // kPerWarp nw-th
+  constexpr int kPerWarp = 32 / kPackGroup;
+  c = sp.big + kPerWarp * (nw - 1 - gw) + lane / kPackGroup;
+  if (c < sp.total) cp = a.copies[c];
+  for (; c < sp.total; c += kPerWarp * nw) {
+    const PackCopy cur = cp;
+    if (c + kPerWarp * nw < sp.total) cp = a.copies[c + kPerWarp * nw];
+    pack_one<T, kPackGroup, kPackGroupU>(c < sp.small_a ? a : b, cur, lane % kPackGroup);
   }
 }
 
@@ -508,16 +532,18 @@ int fp64_max_ctas_per_sm(bool tail_only) {
   return e == cudaSuccess && n > 0 ? n : 1;
 }
 
-cudaError_t launch_pack2(const PackParams &a, const PackParams &b, int32_t ntotal, int sms, cudaStream_t s) {
-  if (ntotal <= 0) return cudaSuccess;
+cudaError_t launch_pack2(const PackParams &a, const PackParams &b, const PackSplit &split, int sms, cudaStream_t s) {
+  if (split.total <= 0) return cudaSuccess;
   // eight CTAs per SM, about two waves at this kernel's occupancy: the copies
   // are dealt to the warps in turn, and the second wave's warps pick up the
   // shares of the first wave's slowest (measured faster than one wave)
   int grid = std::max(1, sms) * 8;
-  const int need = (ntotal + 7) / 8;   // one warp per copy, eight warps a CTA
-  grid = grid < need ? grid : need;
-  if (a.elem_bytes == 8) pack_kernel<double><<<grid, 256, 0, s>>>(a, b, ntotal);
-  else pack_kernel<uint16_t><<<grid, 256, 0, s>>>(a, b, ntotal);
+  constexpr int64_t kPerWarp = 32 / kPackGroup;
+  const int64_t warps = split.big + ((int64_t)split.total - split.big + kPerWarp - 1) / kPerWarp;
+  const int64_t need = (warps + 7) / 8;   // eight warps a CTA
+  grid = grid < need ? grid : (int)need;
+  if (a.elem_bytes == 8) pack_kernel<double><<<grid, 256, 0, s>>>(a, b, split);
+  else pack_kernel<uint16_t><<<grid, 256, 0, s>>>(a, b, split);
   return cudaGetLastError();
 }
 

@@ -171,6 +171,16 @@ struct PackParams {
   int32_t elem_bytes;
 };
 
+// The gather's copy list in four runs: [0, big_a) A's copies moved by whole
+// warps, [big_a, big) B's; [big, small_a) A's small copies (at most
+// kPackSmallElems elements) moved by 8-lane groups, four to a warp, and
+// [small_a, total) B's.
+constexpr int32_t kPackSmallElems = 64;
+struct PackSplit {
+  int32_t big_a, big, small_a, total;
+  bool of_a(int64_t t) const { return t < big_a || (t >= big && t < small_a); }
+};
+
 // ---- BF16 tensor-core path ------------------------------------------------
 // One task = a 128 x BN tile of a contraction-axis group; its K loop walks the
 // group's block pairs, each with its own tensor maps (zero fill past the block

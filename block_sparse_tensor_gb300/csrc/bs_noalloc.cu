@@ -139,12 +139,12 @@ extern "C" bs_status bs_contract_noalloc(const bs_plan *P, const void *A, const 
     pa.src = A;
     pa.dst = b + o_ws_a;
     pa.copies = (const PackCopy *)(b + o_pack);
-    pa.ncopies = P->pack_copies_a;
+    pa.ncopies = P->pack_split.total;
     pa.elem_bytes = 8;
     PackParams pb = pa;
     pb.src = B;
     pb.dst = b + o_ws_b;
-    if (launch_pack2(pa, pb, (int32_t)P->pack_copies.size(), sms, s) != cudaSuccess) return BS_ERR_CUDA;
+    if (launch_pack2(pa, pb, P->pack_split, sms, s) != cudaSuccess) return BS_ERR_CUDA;
   }
   if (!P->zero_blocks.empty() &&
       launch_zero(C, 8, (const ZeroBlock *)(b + o_zero), (int)P->zero_blocks.size(), sms * 4, s) != cudaSuccess)

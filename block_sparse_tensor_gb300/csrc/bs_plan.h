@@ -117,8 +117,8 @@ struct bs_plan {
   int32_t axis = BS_AXIS_CONTRACTION;
   bs::GroupSet gs;
   bs::TileSet ts;
-  std::vector<bs::PackCopy> pack_copies;   // A copies first, then B copies
-  int32_t pack_copies_a = 0;
+  std::vector<bs::PackCopy> pack_copies;   // whole-warp copies of A then B, then small copies of A then B
+  bs::PackSplit pack_split{};
   std::vector<bs::ZeroBlock> zero_blocks;
   // BF16 path
   std::vector<bs::Bf16Task> btasks;   // plan order (longest first)
