@@ -369,6 +369,25 @@ def test_fp64_tile_path_integer_inputs_bit_exact(seed, pol, lay):
     compare(r, r.run(), exact=True)
 
 
+@pytest.mark.parametrize("seed", range(3))
+@pytest.mark.parametrize("lay", [("blockrow", "blockrow"), ("blockrow|charge_sorted", "rowpanel"),
+                                 ("colpanel", "blockrow|charge_sorted")])
+def test_fp64_gather_every_alignment_integer_inputs_bit_exact(seed, lay):
+    """The gather into panels on dimensions of both parities, from 1 to 300: blocks
+    whose rows are 1 to 300 doubles, source and destination rows starting on or 8
+    bytes off a 16-byte boundary, flat runs of both lengths' parities, runs under
+    and over 64 elements and of more than 2048 (banded), and copies of at most 64
+    elements.  Every path of the gather is taken; integer inputs, so C must match
+    the oracle bit for bit."""
+    rng = np.random.default_rng(300 + seed)
+    dims = lambda n: [int(x) for x in rng.choice([1, 2, 3, 5, 8, 63, 64, 65, 130, 131, 257, 300], n)]
+    w = _int_workload(seed, "f64", dims(6), dims(7), dims(5), f"int_gather_{seed}")
+    r = Run(w, lay[0], lay[1], "rowpanel", axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)
+    st = r.P.stats()
+    assert st["packed_a"] == 1 and st["packed_b"] == 1
+    compare(r, r.run(), exact=True)
+
+
 @pytest.mark.parametrize("seed", range(4))
 def test_bf16_multi_tile_integer_inputs_bit_exact(seed):
     """Groups of several 128-row M tiles, tile widths of 192 to 256 columns plus a
