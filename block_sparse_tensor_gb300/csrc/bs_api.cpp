@@ -114,6 +114,68 @@ void pack_list(const bs_layout &src, const bs_layout &dst, std::vector<PackCopy>
   for (const auto &c : all) ((int64_t)c.rows * c.cols <= kPackSmallElems ? small : big)->push_back(c);
 }
 
+// The same gather as shared-memory segments: every block of the source
+// layout becomes pieces (bands of rows spanning at most kSegElems source
+// elements, or row chunks of at most kSegElems columns when one row is
+// longer), and pieces taken in source order fill segments while the span from
+// the segment's first element to the end of its last piece stays within
+// kSegElems and it holds at most kSegPieces of them.
+void seg_list(const bs_layout &src, const bs_layout &dst, int32_t operand, std::vector<PackSeg> *segs,
+              std::vector<PackPiece> *pieces) {
+  struct Placed {
+    int64_t src;   // first source element
+    PackPiece p;
+  };
+  std::vector<Placed> ps;
+  for (const auto &b : src.blocks) {
+    const auto &d = dst.blocks[dst.find(b.row, b.col)];
+    if (b.cols > kSegElems) {
+      for (int32_t r = 0; r < b.rows; ++r)
+        for (int32_t c0 = 0; c0 < b.cols; c0 += kSegElems) {
+          PackPiece p{};
+          p.dst = d.offset + (int64_t)r * d.ld + c0;
+          p.rows = 1;
+          p.cols = std::min(kSegElems, b.cols - c0);
+          p.src_ld = p.dst_ld = p.cols;
+          ps.push_back({b.offset + (int64_t)r * b.ld + c0, p});
+        }
+      continue;
+    }
+    // h rows span (h - 1) ld + cols <= kSegElems source elements
+    const int32_t h = (int32_t)std::max<int64_t>(1, std::min<int64_t>(b.rows, (kSegElems - b.cols) / b.ld + 1));
+    for (int32_t r0 = 0; r0 < b.rows; r0 += h) {
+      PackPiece p{};
+      p.dst = d.offset + (int64_t)r0 * d.ld;
+      p.rows = std::min(h, b.rows - r0);
+      p.cols = b.cols;
+      p.src_ld = (int32_t)b.ld;
+      p.dst_ld = (int32_t)d.ld;
+      ps.push_back({b.offset + (int64_t)r0 * b.ld, p});
+    }
+  }
+  std::stable_sort(ps.begin(), ps.end(), [](const Placed &x, const Placed &y) { return x.src < y.src; });
+  for (size_t i = 0; i < ps.size();) {
+    PackSeg s{};
+    s.src = ps[i].src;
+    s.piece_begin = (int32_t)pieces->size();
+    s.operand = operand;
+    int64_t end = s.src;
+    size_t j = i;
+    for (; j < ps.size() && j - i < (size_t)kSegPieces; ++j) {
+      const int64_t qend = ps[j].src + (int64_t)(ps[j].p.rows - 1) * ps[j].p.src_ld + ps[j].p.cols;
+      if (j > i && qend - s.src > kSegElems) break;
+      PackPiece p = ps[j].p;
+      p.src_off = (int32_t)(ps[j].src - s.src);
+      pieces->push_back(p);
+      end = std::max(end, qend);
+    }
+    s.n = (int32_t)(end - s.src);
+    s.piece_count = (int32_t)(j - i);
+    segs->push_back(s);
+    i = j;
+  }
+}
+
 void zero_list(const bs_layout &C, const std::vector<uint8_t> *cmask, std::vector<ZeroBlock> *out) {
   for (size_t t = 0; t < C.blocks.size(); ++t) {
     if (cmask && !(*cmask)[t]) continue;   // another shard's C block
@@ -301,6 +363,8 @@ bs_status upload(bs_plan *P) {
   size_t o_tail = append_bytes(buf, P->ts.tail_elems);
   size_t o_tdesc = append_bytes(buf, P->ts.tdesc);
   size_t o_pack = append_bytes(buf, P->pack_copies);
+  size_t o_segs = append_bytes(buf, P->pack_segs);
+  size_t o_pieces = append_bytes(buf, P->pack_pieces);
   size_t o_zero = append_bytes(buf, P->zero_blocks);
   size_t o_bc = append_bytes(buf, P->bctas);
   size_t o_bt = append_bytes(buf, P->bstasks);
@@ -320,6 +384,8 @@ bs_status upload(bs_plan *P) {
   P->d_tail = (int32_t *)(b + o_tail);
   P->d_tdesc = (TailDesc *)(b + o_tdesc);
   P->d_pack = (PackCopy *)(b + o_pack);
+  P->d_segs = (PackSeg *)(b + o_segs);
+  P->d_pieces = (PackPiece *)(b + o_pieces);
   P->d_zero = (ZeroBlock *)(b + o_zero);
   P->d_bctas = (Bf16Cta *)(b + o_bc);
   P->d_bstasks = (Bf16Task *)(b + o_bt);
@@ -732,11 +798,21 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
       P->pack_split.small_a = (int32_t)std::min<size_t>(big_a.size() + big_b.size() + small_a.size(), INT32_MAX);
       P->pack_split.total = (int32_t)std::min<size_t>(pc.size(), INT32_MAX);
     }
+    if (dtype == BS_F64) {
+      if (P->pack_a) seg_list(P->A, P->A_pk, 0, &P->pack_segs, &P->pack_pieces);
+      if (P->pack_b) seg_list(P->B, P->B_pk, 1, &P->pack_segs, &P->pack_pieces);
+      // only a gather whose segments fit every SM's stages at once goes by segments
+      if (P->pack_segs.size() > (size_t)std::max(1, P->sm_count) * kSegStages) {
+        P->pack_segs.clear();
+        P->pack_pieces.clear();
+      }
+    }
     {
       // every table the kernels index with 32 bits
       const size_t lim = (size_t)(INT32_MAX - kThreads);
       if (P->ts.tail_elems.size() / 2 > lim || P->ts.tasks.size() > lim || P->gs.groups.size() > lim ||
           P->gs.rsegs.size() > lim || P->gs.ksegs.size() > lim || P->pack_copies.size() > lim ||
+          P->pack_segs.size() > lim || P->pack_pieces.size() > lim ||
           P->btasks.size() > lim || P->bstages.size() > lim) {
         delete P;
         return BS_ERR_OVERFLOW;
@@ -1110,7 +1186,34 @@ static bs_status contract_impl(bs_plan *P, const void *A, const void *B, void *C
     PackParams pb = pp;
     pb.src = B;
     pb.dst = P->d_ws_b;
-    BS_CUDA(launch_pack2(pp, pb, P->pack_split, P->sm_count, s));
+    // A small FP64 gather goes by shared-memory segments: when every SM's
+    // share of segments fits its stages, all its copies are issued at once
+    // and no load waits on another (the tail workload's block-row gather:
+    // 9.9 against 18.0 us).  A larger one goes block copy by block copy,
+    // where the segment writers fell behind (the stress workload's: 212
+    // against 113 us).  So does any gather whose operand buffers do not
+    // start on 16-byte boundaries, and the checked instance, whose reads must
+    // stay within the caller's declared sizes.
+    uintptr_t bases = 0;
+    if (P->pack_a) bases |= (uintptr_t)A;
+    if (P->pack_b) bases |= (uintptr_t)B;
+    if (!P->pack_segs.empty() && !sizes && (bases & 15u) == 0) {
+      SegParams sp{};
+      sp.src[0] = (const double *)A;
+      sp.src[1] = (const double *)B;
+      sp.dst[0] = (double *)P->d_ws_a;
+      sp.dst[1] = (double *)P->d_ws_b;
+      sp.src_nelems[0] = P->A.nelems;
+      sp.src_nelems[1] = P->B.nelems;
+      sp.segs = P->d_segs;
+      sp.pieces = P->d_pieces;
+      sp.nseg = (int32_t)P->pack_segs.size();
+      sp.status = P->d_status;
+      sp.timeout_ns = (uint64_t)(P->opts.wait_timeout_ms > 0 ? P->opts.wait_timeout_ms : 2000) * 1000000ull;
+      BS_CUDA(launch_seg_gather(sp, P->sm_count, s));
+    } else {
+      BS_CUDA(launch_pack2(pp, pb, P->pack_split, P->sm_count, s));
+    }
   }
   if (prof) BS_CUDA(cudaEventRecord(P->ev[1], s));
   if (!P->zero_blocks.empty())

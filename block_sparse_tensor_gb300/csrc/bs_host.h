@@ -53,6 +53,9 @@ Sparsity rule_sparsity(const AxisCopy &r, const AxisCopy &c, const bs_rule &rule
 cudaError_t launch_fp64_grouped(const Fp64Params &p, int grid, cudaStream_t s);
 // The gather of both operands in one launch, eight CTAs per SM of `sms`.
 cudaError_t launch_pack2(const PackParams &a, const PackParams &b, const PackSplit &split, int sms, cudaStream_t s);
+// The FP64 gather by segments (every base pointer 16-byte aligned), one CTA
+// per SM of `sms`.
+cudaError_t launch_seg_gather(const SegParams &p, int sms, cudaStream_t s);
 cudaError_t launch_zero(void *C, int elem_bytes, const ZeroBlock *blocks, int nblocks, int grid,
                         cudaStream_t s);
 // Copies n0 bytes src0 -> dst0 and n1 bytes src1 -> dst1 in one launch; every pointer 16-byte aligned.

@@ -181,6 +181,42 @@ struct PackSplit {
   bool of_a(int64_t t) const { return t < big_a || (t >= big && t < small_a); }
 };
 
+// The FP64 gather in shared-memory segments: a segment is a source range of
+// at most kSegElems elements (consecutive blocks of the source layout, or a
+// band or row chunk of one block) that one bulk copy brings into shared
+// memory, with the pieces it holds (a block, or a band or row chunk of one)
+// and where each goes in the destination.  Segments are listed in source
+// order, A's first.
+constexpr int32_t kSegElems = 2048;
+constexpr int32_t kSegPieces = 128;   // pieces a segment holds at most
+constexpr int32_t kSegStages = 10;    // segments in flight per SM
+struct PackPiece {
+  int64_t dst;       // first destination element
+  int32_t src_off;   // first source element, counted from the segment's first
+  int32_t rows, cols;
+  int32_t src_ld, dst_ld;
+  int32_t pad_;
+};
+static_assert(sizeof(PackPiece) == 32, "piece record");
+struct PackSeg {
+  int64_t src;   // first source element
+  int32_t n;     // elements from src to the end of its last piece
+  int32_t piece_begin, piece_count;
+  int32_t operand;   // 0: A, 1: B
+  int64_t pad_;
+};
+static_assert(sizeof(PackSeg) == 32, "segment record");
+struct SegParams {
+  const double *src[2];    // A, B
+  double *dst[2];          // their panel workspaces
+  int64_t src_nelems[2];   // elements the caller's A and B buffers hold (the layouts' counts)
+  const PackSeg *segs;
+  const PackPiece *pieces;
+  int32_t nseg;
+  int32_t *status;
+  uint64_t timeout_ns;
+};
+
 // ---- BF16 tensor-core path ------------------------------------------------
 // One task = a 128 x BN tile of a contraction-axis group; its K loop walks the
 // group's block pairs, each with its own tensor maps (zero fill past the block

@@ -118,6 +118,8 @@ struct bs_plan {
   bs::GroupSet gs;
   bs::TileSet ts;
   std::vector<bs::PackCopy> pack_copies;   // whole-warp copies of A then B, then small copies of A then B
+  std::vector<bs::PackSeg> pack_segs;      // the same gather as shared-memory segments (FP64 plans)
+  std::vector<bs::PackPiece> pack_pieces;
   bs::PackSplit pack_split{};
   std::vector<bs::ZeroBlock> zero_blocks;
   // BF16 path
@@ -145,6 +147,8 @@ struct bs_plan {
   bs::TailDesc *d_tdesc = nullptr;
   size_t counter_bytes = 256;
   bs::PackCopy *d_pack = nullptr;
+  bs::PackSeg *d_segs = nullptr;
+  bs::PackPiece *d_pieces = nullptr;
   bs::ZeroBlock *d_zero = nullptr;
   bs::Bf16Cta *d_bctas = nullptr;
   bs::Bf16Task *d_bstasks = nullptr;
