@@ -386,7 +386,8 @@ def gather_record(bs, torch, flush, stream, peaks):
     phase events: bytes moved = 2 x packed bytes (each element read and written once)."""
     hbm = peaks.get("hbm_gbs") or 6800.0
     out = {}
-    for n, opts in ((5, dict(axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)), (4, {})):
+    for n, opts in ((5, dict(axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)),
+                    (2, dict(axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)), (4, {})):
         w = bsgen.get(n)
         w.layout_a, w.layout_b, w.layout_c = w.pack_layout_a, w.pack_layout_b, w.pack_layout_c
         pb = Problem(bs, torch, w, profile=1, **opts)
