@@ -89,10 +89,14 @@ int64_t populated_elems(const bs_layout &L) {
 }
 
 // Block copies of the gather, split into row bands of at most 2048 elements
-// so one huge block does not serialise the launch on a few warps, and listed
-// largest first so the warps that take them in turn get equal shares.  Copies
-// of at most kPackSmallElems elements go to `small` (moved four to a warp).
-void pack_list(const bs_layout &src, const bs_layout &dst, std::vector<PackCopy> *big, std::vector<PackCopy> *small) {
+// so one huge block does not serialise the launch on a few warps.  Copies of
+// doubles are listed in destination order, so that the warps that take them
+// in turn write neighbouring pieces of a panel row close together in time
+// (their partial sectors meet in L2); copies of 2-byte elements largest
+// first, for equal shares.  Copies of at most kPackSmallElems elements go to
+// `small` (moved four to a warp).
+void pack_list(const bs_layout &src, const bs_layout &dst, int elem_bytes, std::vector<PackCopy> *big,
+               std::vector<PackCopy> *small) {
   std::vector<PackCopy> all;
   for (const auto &b : src.blocks) {
     const auto &d = dst.blocks[dst.find(b.row, b.col)];
@@ -108,9 +112,12 @@ void pack_list(const bs_layout &src, const bs_layout &dst, std::vector<PackCopy>
       all.push_back(c);
     }
   }
-  std::stable_sort(all.begin(), all.end(), [](const PackCopy &x, const PackCopy &y) {
-    return (int64_t)x.rows * x.cols > (int64_t)y.rows * y.cols;
-  });
+  if (elem_bytes == 8)
+    std::stable_sort(all.begin(), all.end(), [](const PackCopy &x, const PackCopy &y) { return x.dst < y.dst; });
+  else
+    std::stable_sort(all.begin(), all.end(), [](const PackCopy &x, const PackCopy &y) {
+      return (int64_t)x.rows * x.cols > (int64_t)y.rows * y.cols;
+    });
   for (const auto &c : all) ((int64_t)c.rows * c.cols <= kPackSmallElems ? small : big)->push_back(c);
 }
 
@@ -788,8 +795,9 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
     }
     {
       std::vector<PackCopy> big_a, small_a, big_b, small_b;
-      if (P->pack_a) pack_list(P->A, P->A_pk, &big_a, &small_a);
-      if (P->pack_b) pack_list(P->B, P->B_pk, &big_b, &small_b);
+      const int eb = P->dtype == BS_F64 ? 8 : 2;
+      if (P->pack_a) pack_list(P->A, P->A_pk, eb, &big_a, &small_a);
+      if (P->pack_b) pack_list(P->B, P->B_pk, eb, &big_b, &small_b);
       auto &pc = P->pack_copies;
       pc.clear();
       for (const auto *v : {&big_a, &big_b, &small_a, &small_b}) pc.insert(pc.end(), v->begin(), v->end());
