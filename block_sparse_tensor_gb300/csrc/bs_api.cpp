@@ -809,8 +809,9 @@ static bs_status plan_create(const bs_layout *A, const bs_layout *B, const bs_la
     if (dtype == BS_F64) {
       if (P->pack_a) seg_list(P->A, P->A_pk, 0, &P->pack_segs, &P->pack_pieces);
       if (P->pack_b) seg_list(P->B, P->B_pk, 1, &P->pack_segs, &P->pack_pieces);
-      // only a gather whose segments fit every SM's stages at once goes by segments
-      if (P->pack_segs.size() > (size_t)std::max(1, P->sm_count) * kSegStages) {
+      // only a small gather goes by segments (measured on block-row gathers of
+      // stress-like workloads: faster up to 1.2 segments per SM, slower from 3.3)
+      if (P->pack_segs.size() > (size_t)std::max(1, P->sm_count) * kSegMaxPerSm) {
         P->pack_segs.clear();
         P->pack_pieces.clear();
       }
@@ -1194,14 +1195,14 @@ static bs_status contract_impl(bs_plan *P, const void *A, const void *B, void *C
     PackParams pb = pp;
     pb.src = B;
     pb.dst = P->d_ws_b;
-    // A small FP64 gather goes by shared-memory segments: when every SM's
-    // share of segments fits its stages, all its copies are issued at once
-    // and no load waits on another (the tail workload's block-row gather:
-    // 9.9 against 18.0 us).  A larger one goes block copy by block copy,
-    // where the segment writers fell behind (the stress workload's: 212
-    // against 113 us).  So does any gather whose operand buffers do not
-    // start on 16-byte boundaries, and the checked instance, whose reads must
-    // stay within the caller's declared sizes.
+    // A small FP64 gather (at most two segments per SM) goes by shared-memory
+    // segments: all its copies are issued at once and no load waits on
+    // another (the tail workload's block-row gather: 9.9 against 18.0 us).
+    // A larger one goes block copy by block copy, where the segment writers
+    // fall behind (the stress workload's: 207 against 111 us).  So does any
+    // gather whose operand buffers do not start on 16-byte boundaries, and
+    // the checked instance, whose reads must stay within the caller's
+    // declared sizes.
     uintptr_t bases = 0;
     if (P->pack_a) bases |= (uintptr_t)A;
     if (P->pack_b) bases |= (uintptr_t)B;

@@ -190,6 +190,7 @@ struct PackSplit {
 constexpr int32_t kSegElems = 2048;
 constexpr int32_t kSegPieces = 128;   // pieces a segment holds at most
 constexpr int32_t kSegStages = 10;    // segments in flight per SM
+constexpr int32_t kSegMaxPerSm = 2;   // a plan gathers by segments only up to this many per SM
 struct PackPiece {
   int64_t dst;       // first destination element
   int32_t src_off;   // first source element, counted from the segment's first
