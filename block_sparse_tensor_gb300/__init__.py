@@ -35,7 +35,7 @@ EXPORTED = ["bs_layout_create", "bs_layout_query", "bs_layout_blocks", "bs_layou
             "bs_contract_uncoalesced", "bs_plan_last_device_error", "bs_plan_destroy",
             "bs_status_string", "bs_version", "bs_calibrate", "bs_contract_noalloc",
             "bs_plan_check_groups", "bs_plan_create_into", "bs_plan_profile", "bs_plan_create_shard",
-            "bs_plan_operand_blocks", "bs_calibration_apply", "bs_contract_checked"]
+            "bs_plan_operand_blocks", "bs_calibration_apply", "bs_contract_checked", "bs_plan_gather_segments"]
 
 
 class BsError(RuntimeError):
@@ -134,6 +134,7 @@ def _load(path: str = LIB_PATH):
         "bs_plan_operand_blocks": (st, [P, i32, P, P]),
         "bs_calibration_apply": (None, [P, P]),
         "bs_contract_checked": (st, [P, P, i64, P, i64, P, i64, P]),
+        "bs_plan_gather_segments": (st, [P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -294,6 +295,17 @@ class Plan:
         out = np.zeros((max(n.value, 1), 8), np.int64)
         _check(lib.bs_plan_groups(self.h, ctypes.byref(n), out.ctypes.data), "bs_plan_groups")
         return out[:n.value]
+
+    def gather_segments(self):
+        """(segments, pieces) of bs_plan_gather_segments: an (n, 5) and an (m, 6) int64 array."""
+        ns, npc = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib.bs_plan_gather_segments(self.h, ctypes.byref(ns), ctypes.byref(npc), None, None),
+               "bs_plan_gather_segments")
+        segs = np.zeros((max(ns.value, 1), 5), np.int64)
+        pcs = np.zeros((max(npc.value, 1), 6), np.int64)
+        _check(lib.bs_plan_gather_segments(self.h, ctypes.byref(ns), ctypes.byref(npc), segs.ctypes.data,
+                                           pcs.ctypes.data), "bs_plan_gather_segments")
+        return segs[:ns.value], pcs[:npc.value]
 
     def check_groups(self):
         """(status, first failing group or -1) of bs_plan_check_groups."""

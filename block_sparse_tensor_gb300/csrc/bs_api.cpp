@@ -1011,6 +1011,35 @@ bs_status bs_plan_groups(const bs_plan *P, int64_t *ngroups, int64_t *out) {
   return BS_OK;
 }
 
+bs_status bs_plan_gather_segments(const bs_plan *P, int64_t *nseg, int64_t *npieces, int64_t *seg_out,
+                                  int64_t *piece_out) {
+  if (!P || !nseg || !npieces) return BS_ERR_INVALID_ARG;
+  *nseg = (int64_t)P->pack_segs.size();
+  *npieces = (int64_t)P->pack_pieces.size();
+  if (seg_out)
+    for (size_t s = 0; s < P->pack_segs.size(); ++s) {
+      const PackSeg &g = P->pack_segs[s];
+      int64_t *o = seg_out + 5 * s;
+      o[0] = g.src;
+      o[1] = g.n;
+      o[2] = g.piece_begin;
+      o[3] = g.piece_count;
+      o[4] = g.operand;
+    }
+  if (piece_out)
+    for (size_t p = 0; p < P->pack_pieces.size(); ++p) {
+      const PackPiece &c = P->pack_pieces[p];
+      int64_t *o = piece_out + 6 * p;
+      o[0] = c.dst;
+      o[1] = c.src_off;
+      o[2] = c.rows;
+      o[3] = c.cols;
+      o[4] = c.src_ld;
+      o[5] = c.dst_ld;
+    }
+  return BS_OK;
+}
+
 bs_status bs_plan_triples(const bs_plan *P, int64_t *ntriples, int64_t *ngroups, int64_t *group_ptr, int32_t *out) {
   if (!P || !ntriples || !ngroups) return BS_ERR_INVALID_ARG;
   std::vector<int64_t> tp;

@@ -297,6 +297,20 @@ bs_status bs_plan_profile(bs_plan *plan, bs_phase_times *out);
  * Call with out = NULL to get the count in *ngroups. */
 bs_status bs_plan_groups(const bs_plan *plan, int64_t *ngroups, int64_t *out);
 
+/* The FP64 gather's shared-memory segments, for inspection ("Interleaved vs
+ * contiguous" of the uni20 note: the pack that makes fragmented operands
+ * contiguous).  A plan that gathers at most two segments per SM keeps them and
+ * gathers by them; otherwise *nseg is 0 (it gathers block copy by block copy).
+ * For segment s, seg_out[5*s .. 5*s+4] = {first source element, source
+ * elements it spans (at most 2048), first piece, pieces (at most 128), operand
+ * (0 A, 1 B)}, segments of A first, each operand's in source order; for piece
+ * p, piece_out[6*p .. 6*p+5] = {first destination element in the operand's
+ * panel workspace, first source element counted from its segment's first,
+ * rows, cols, source ld, destination ld}.  Pass NULL arrays to get the counts.
+ * Host only, reads no device memory. */
+bs_status bs_plan_gather_segments(const bs_plan *plan, int64_t *nseg, int64_t *npieces, int64_t *seg_out,
+                                  int64_t *piece_out);
+
 /* Triple coverage for inspection: for each group, the (i, k, j) triples it
  * computes, as out[3*t .. 3*t+2], group by group; group_ptr[g] .. group_ptr[g+1]
  * delimit group g.  Pass NULL arrays to get the sizes. */

@@ -217,6 +217,66 @@ def test_blockrow_layout_fragments_groups_and_pack_merges_them():
     assert st["packed_a"] == 1 and st["packed_b"] == 1 and st["packed_bytes"] > 0
 
 
+def _gather_map(src_layout, dst_layout):
+    """(source element, destination element) of every populated element: block (r, c)
+    of the source layout goes to block (r, c) of the panel layout, row by row."""
+    from harness import element_index
+    sb, db = src_layout.blocks(), dst_layout.blocks()
+    key = {(int(b[0]), int(b[1])): i for i, b in enumerate(db)}
+    db = db[[key[(int(b[0]), int(b[1]))] for b in sb]]
+    return element_index(sb), element_index(db)
+
+
+@pytest.mark.parametrize("case", ["tail", "tiny0", "tiny2", "tiny3", "mixed"])
+def test_gather_segments_move_every_element_once(case):
+    """The segments of an FP64 gather: each spans at most 2048 source elements and
+    holds at most 128 pieces, each piece lies inside its segment, each operand's
+    segments come in source order, and the pieces together send every populated
+    source element to its place in the panel exactly once."""
+    if case == "tail":
+        w, la, lb = bsgen.config2(), "blockrow", "blockrow"
+    elif case == "mixed":
+        w, la, lb = bsgen.config2(), "colpanel", "blockrow|charge_sorted"
+    else:
+        w = bsgen.tiny_random(700 + int(case[-1]), max_sectors=12, max_dim=300)
+        la, lb = "blockrow", "blockrow|align16"
+    P, A, B = host_plan(w, la, lb, axis_policy=bs.AXIS_CONTRACTION, pack_policy=bs.PACK_ALWAYS)
+    segs, pcs = P.gather_segments()
+    assert len(segs) > 0 and len(segs) <= 2 * 152
+    assert np.all(segs[:, 1] <= 2048) and np.all((segs[:, 3] >= 1) & (segs[:, 3] <= 128))
+    assert segs[:, 3].sum() == len(pcs) and np.array_equal(segs[:, 2], np.concatenate([[0], np.cumsum(segs[:-1, 3])]))
+    for op, (L, flags) in enumerate([(A, "rowpanel|charge_sorted"), (B, "colpanel|charge_sorted")]):
+        so = segs[segs[:, 4] == op]
+        assert np.all(np.diff(so[:, 0]) > 0)
+        seg_src, seg_dst = [], []
+        for first, n, p0, npc, _ in so:
+            for dst, off, rows, cols, sld, dld in pcs[p0:p0 + npc]:
+                assert 0 <= off and off + (rows - 1) * sld + cols <= n
+                r, c = np.divmod(np.arange(rows * cols), cols)
+                seg_src.append(first + off + r * sld + c)
+                seg_dst.append(dst + r * dld + c)
+        got_src, got_dst = np.concatenate(seg_src), np.concatenate(seg_dst)
+        assert len(np.unique(got_src)) == len(got_src), "a source element is moved twice"
+        if op == 0:
+            pk = bs.Layout(w.rows, w.inner, w.rule_a, flags, 8)
+        else:
+            pk = bs.Layout(w.inner, w.cols, w.rule_b, flags, 8)
+        want_src, want_dst = _gather_map(L, pk)
+        o1, o2 = np.argsort(got_src), np.argsort(want_src)
+        assert np.array_equal(got_src[o1], want_src[o2])
+        assert np.array_equal(got_dst[o1], want_dst[o2])
+
+
+def test_large_gathers_keep_no_segments():
+    """The stress workload's block-row gather (about 98 segments per SM) goes block
+    copy by block copy: the plan keeps no segment tables."""
+    w = bsgen.config5()
+    P, _, _ = host_plan(w, w.pack_layout_a, w.pack_layout_b, axis_policy=bs.AXIS_CONTRACTION,
+                        pack_policy=bs.PACK_ALWAYS)
+    segs, pcs = P.gather_segments()
+    assert len(segs) == 0 and len(pcs) == 0 and P.stats()["packed_a"] == 1
+
+
 def test_bf16_misaligned_views_are_packed_or_refused():
     w = bsgen.config4()
     P, _, _ = host_plan(w, "blockrow", "blockrow")
