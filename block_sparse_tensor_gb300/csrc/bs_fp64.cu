@@ -367,8 +367,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) fp64_grouped_kernel(Fp64Pa
   }
 }
 
-// The gather: one warp per block copy, copies listed largest first at plan
-// time and dealt to the warps in turn (each warp fetches its next copy's
+// The gather: one warp per block copy, copies listed at plan time (doubles in
+// destination order, 2-byte elements largest first) and dealt to the warps
+// in turn (each warp fetches its next copy's
 // descriptor while it moves the current one); then the small copies (at most
 // kPackSmallElems elements), four to a warp, 8 lanes each, so that a warp has
 // four of them in flight instead of waiting on each in turn.  A copy is moved
